@@ -1,0 +1,465 @@
+"""Pins of the CPU oracle to facts other than itself (run without a GPU).
+
+Each test checks the oracle against something the method's description or
+plain mathematics fixes: closed forms, textbook special cases computed by a
+library routine (numpy, torch), brute force on tiny inputs, finite
+differences, the Figure 1 worked layout. The method is the one on the Pith
+review page of arXiv 2512.16615 ("Core claim", "What carries the argument",
+referee report on Algorithm 1 / Eq. (6) / KV Reweighting, Figure 1).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from hierarchical_sparse_attention_mean_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def rng_inputs(n, d, seed, amp=1.0, bh=1):
+    w = synth.small("pin", 1, bh, n, d, dtype="fp32", amplitude=amp, seed=seed)
+    return synth.make_inputs(w, threads=1)
+
+
+def direct_mean_pyramid(x, B, L):
+    """Level l as the plain mean of B^l consecutive rows (not the recursion)."""
+    n, d = x.shape
+    out = []
+    for l in range(1, L + 1):
+        out.append(np.asarray(x, np.float64).reshape(n // B ** l, B ** l, d).mean(axis=1))
+    return np.concatenate(out)
+
+
+def brute_topk(scores, cand, K):
+    """Top-K by counting, for every candidate, how many others outrank it
+    (higher score, or equal score with lower index)."""
+    scores = np.asarray(scores)
+    cand = np.asarray(cand)
+    keep, top1 = [], None
+    for a in range(len(cand)):
+        rank = sum(1 for b in range(len(cand))
+                   if scores[b] > scores[a] or (scores[b] == scores[a] and cand[b] < cand[a]))
+        if rank < K:
+            keep.append(int(cand[a]))
+        if rank == 0:
+            top1 = int(cand[a])
+    return sorted(keep), top1
+
+
+def dense_masked(q, k, v, B, L, Le, sel, coarse, scale):
+    """Brute-force attention: one dense logit matrix over all n fine tokens and
+    all pooled tokens of levels 1..Le, masked to the sparse key set (0 / -inf)
+    plus ln(B^l) on the coarse columns; softmax by logsumexp."""
+    q64, k64, v64 = (np.asarray(a, np.float64) for a in (q, k, v))
+    n, d = q64.shape
+    kp, vp = direct_mean_pyramid(k, B, L), direct_mean_pyramid(v, B, L)
+    sizes = oracle.level_sizes(n, B, L)
+    offs = np.cumsum([0] + sizes[1:])
+    keys = [k64] + [kp[offs[l - 1]:offs[l]] for l in range(1, Le + 1)]
+    vals = [v64] + [vp[offs[l - 1]:offs[l]] for l in range(1, Le + 1)]
+    K_all, V_all = np.concatenate(keys), np.concatenate(vals)
+    logits = scale * q64 @ K_all.T
+    mask = np.full(logits.shape, -np.inf)
+    col0 = np.cumsum([0] + [a.shape[0] for a in keys])
+    for t in range(n):
+        i = t // B
+        for j in sel[i]:
+            mask[t, j * B:(j + 1) * B] = 0.0
+        for l in range(1, Le + 1):
+            mask[t, col0[l] + coarse[i, l - 1]] = l * math.log(B)
+    z = logits + mask
+    m = z.max(axis=1, keepdims=True)
+    lse = (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
+    o = np.exp(z - lse[:, None]) @ V_all
+    return o, lse, int(np.isfinite(mask[0]).sum())
+
+
+def run_slice(x, B, K, L=None, Le=None, scale=None, dout=None):
+    n, d = x["q"].shape[-2:]
+    res = oracle.run(x["q"][None] if x["q"].ndim == 2 else x["q"],
+                     x["k"][None] if x["k"].ndim == 2 else x["k"],
+                     x["v"][None] if x["v"].ndim == 2 else x["v"],
+                     dout, B=B, K=K, L=L, Le=Le, scale=scale)
+    return res
+
+
+# ---------------------------------------------------------------- levels ---
+
+def test_num_levels_matches_floor_formula():
+    for B in (2, 3, 4, 8, 16, 64):
+        for n in range(B * B, 5000, 7):
+            expect = int(math.floor(math.log(n) / math.log(B) - 1 + 1e-12))
+            # guard the float formula at exact powers
+            p = B ** (expect + 2)
+            if p <= n:
+                expect += 1
+            assert oracle.num_levels(n, B) == expect, (n, B)
+
+
+def test_fig1_layout_golden():
+    g = json.load(open(os.path.join(GOLDEN, "fig1_layout.json")))
+    N, B, K = g["N"], g["B"], g["K"]
+    L = oracle.num_levels(N, B)
+    assert L == g["L"]
+    assert oracle.level_sizes(N, B, L) == g["level_sizes"]
+    x = rng_inputs(N, 4, seed=3)
+    res = run_slice({k: v[0] for k, v in x.items()}, B, K)
+    s = res["slices"][0]["sel"]
+    # coarsest level: full scoring of its n_L tokens, K kept
+    assert s["levels"][L].shape == (g["level_sizes"][L], K)
+    # level 1: each query token scores K*B children
+    _, _, work = oracle.select_level(res["slices"][0]["qpyr"][:4], res["slices"][0]["kpyr"][:4], B,
+                                     s["levels"][2], K)
+    assert work == g["level_sizes"][1] * g["candidates_per_query_at_level_1"]
+    assert s["levels"][1].shape[1] * B == g["fine_keys_per_query"]
+    assert s["coarse"].shape[1] == g["coarse_keys_per_query"]
+
+
+# ------------------------------------------------------------------ pool ---
+
+@pytest.mark.parametrize("n,B", [(256, 16), (4096, 16), (64, 4), (8, 2), (729, 3)])
+def test_pool_equals_direct_mean(n, B):
+    L = oracle.num_levels(n, B)
+    x = rng_inputs(n, 8, seed=11)["q"][0]
+    got = oracle.pool(x, B, L)
+    np.testing.assert_allclose(got, direct_mean_pyramid(x, B, L), rtol=1e-12, atol=1e-14)
+
+
+def test_pool_constant_and_linear():
+    n, B, d = 4096, 16, 8
+    L = oracle.num_levels(n, B)
+    c = np.full((n, d), 0.375, np.float32)
+    assert np.all(oracle.pool(c, B, L) == 0.375)
+    # bf16-valued inputs keep 2a - b exact in float32
+    a = synth.bf16_round(rng_inputs(n, d, seed=1)["q"][0])
+    b = synth.bf16_round(rng_inputs(n, d, seed=2)["q"][0])
+    comb = (2.0 * a - b).astype(np.float32)
+    assert np.array_equal(comb.astype(np.float64), 2.0 * a.astype(np.float64) - b.astype(np.float64))
+    lhs = oracle.pool(comb, B, L)
+    rhs = 2.0 * oracle.pool(a, B, L) - oracle.pool(b, B, L)
+    np.testing.assert_allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- select ---
+
+def test_single_level_is_textbook_block_topk():
+    """L = 1: one pooled level scored in full, Top-K per row -- the
+    single-level design LLSA generalises."""
+    n, B, K, d = 1024, 16, 4, 16
+    x = rng_inputs(n, d, seed=5)
+    qp = direct_mean_pyramid(x["q"][0], B, 1)
+    kp = direct_mean_pyramid(x["k"][0], B, 1)
+    S = qp @ kp.T
+    res = run_slice({k: v[0] for k, v in x.items()}, B, K)
+    sel = res["slices"][0]["sel"]
+    assert res["L"] == 1
+    for i in range(S.shape[0]):
+        order = np.lexsort((np.arange(S.shape[1]), -S[i]))
+        assert sorted(order[:K].tolist()) == sel["levels"][1][i].tolist()
+        assert sel["top1"][1][i] == order[0]
+        assert sel["coarse"][i, 0] == order[0]
+
+
+@pytest.mark.parametrize("n,B,K", [(256, 4, 3), (512, 2, 2), (4096, 16, 8), (729, 3, 2)])
+def test_hierarchical_select_brute_force(n, B, K):
+    d = 8
+    x = rng_inputs(n, d, seed=n + B)
+    L = oracle.num_levels(n, B)
+    qp = direct_mean_pyramid(x["q"][0], B, L)
+    kp = direct_mean_pyramid(x["k"][0], B, L)
+    sizes = oracle.level_sizes(n, B, L)
+    offs = np.cumsum([0] + sizes[1:])
+    res = run_slice({k: v[0] for k, v in x.items()}, B, K)
+    sel = res["slices"][0]["sel"]
+    for l in range(L, 0, -1):
+        Ql, Kl = qp[offs[l - 1]:offs[l]], kp[offs[l - 1]:offs[l]]
+        for i in range(sizes[l]):
+            if l == L:
+                cand = np.arange(sizes[L])
+            else:
+                cand = np.concatenate([np.arange(j * B, (j + 1) * B) for j in sel["levels"][l + 1][i // B]])
+            keep, top1 = brute_topk(Kl[cand] @ Ql[i], cand, K)
+            assert keep == sel["levels"][l][i].tolist(), (l, i)
+            assert top1 == sel["top1"][l][i]
+    # enrichment token of level l = rank-1 of the level-l ancestor's row
+    for i in range(sizes[1]):
+        for l in range(1, L + 1):
+            assert sel["coarse"][i, l - 1] == sel["top1"][l][i // B ** (l - 1)]
+
+
+def test_hierarchy_invariant_and_work_count():
+    """Every kept fine block descends from a kept block at every coarser
+    level; scored pairs = n_L^2 + sum_{l<L} n_l K_{l+1} B, bounded by the
+    geometric sum n_L^2 + N K B / (B - 1) (Eq. (6))."""
+    for (n, B, K) in [(4096, 16, 8), (65536, 16, 8), (1024, 4, 3), (2048, 2, 2)]:
+        d = 4
+        x = rng_inputs(n, d, seed=9)
+        L = oracle.num_levels(n, B)
+        res = oracle.run(x["q"], x["k"], x["v"], B=B, K=K, backward=False)
+        sel = res["slices"][0]["sel"]
+        sizes = oracle.level_sizes(n, B, L)
+        for i in range(sizes[1]):
+            for j in sel["levels"][1][i]:
+                for l in range(2, L + 1):
+                    assert j // B ** (l - 1) in sel["levels"][l][i // B ** (l - 1)]
+        kl = oracle.level_topk(n, B, L, K)
+        expect = sizes[L] ** 2 + sum(sizes[l] * kl[l + 1] * B for l in range(1, L))
+        assert sel["work"] == expect
+        assert sel["work"] <= sizes[L] ** 2 + n * K * B / (B - 1)
+
+
+def test_full_selection_when_KB_covers_everything():
+    n, B = 1024, 16
+    x = rng_inputs(n, 8, seed=21)
+    res = run_slice({k: v[0] for k, v in x.items()}, B, K=64)
+    sel = res["slices"][0]["sel"]["levels"][1]
+    assert sel.shape == (64, 64)
+    assert (sel == np.arange(64)[None, :]).all()
+    n = 4096  # two levels: K >= n_2 and K*... >= n_1
+    x = rng_inputs(n, 8, seed=22)
+    res = run_slice({k: v[0] for k, v in x.items()}, B, K=256)
+    sel = res["slices"][0]["sel"]["levels"]
+    assert (sel[2] == np.arange(16)).all() and (sel[1] == np.arange(256)).all()
+
+
+def test_planted_block_wins_every_level():
+    """A key block whose keys align with every query is the rank-1 choice at
+    every level; flipping its sign makes it never chosen at the top rank."""
+    n, B, K, d = 4096, 16, 4, 8
+    L = oracle.num_levels(n, B)
+    rng = np.random.default_rng(0)
+    u = np.ones(d, np.float32) / math.sqrt(d)
+    q = (np.tile(u, (n, 1)) + 0.01 * rng.standard_normal((n, d))).astype(np.float32)
+    k = (0.1 * rng.standard_normal((n, d))).astype(np.float32)
+    jstar = 1234 // B  # block 77
+    k[jstar * B:(jstar + 1) * B] += 8.0 * u
+    v = rng.standard_normal((n, d)).astype(np.float32)
+    res = oracle.run(q[None], k[None], v[None], B=B, K=K, backward=False)
+    sel = res["slices"][0]["sel"]
+    for l in range(1, L + 1):
+        anc = jstar // B ** (l - 1)
+        assert (sel["top1"][l] == anc).all(), l
+        assert all(anc in row for row in sel["levels"][l])
+    k2 = k.copy()
+    k2[jstar * B:(jstar + 1) * B] -= 16.0 * u
+    res2 = oracle.run(q[None], k2[None], v[None], B=B, K=K, backward=False)
+    assert not (res2["slices"][0]["sel"]["top1"][1] == jstar).any()
+
+
+def test_ties_go_to_lower_index():
+    n, B, K, d = 4096, 16, 8, 8
+    c = np.ones((n, d), np.float32)
+    res = oracle.run(c[None], c[None], c[None], B=B, K=K, backward=False)
+    sel = res["slices"][0]["sel"]
+    assert (sel["levels"][2] == np.arange(8)).all()     # coarsest: first K tokens
+    assert (sel["levels"][1] == np.arange(8)).all()     # children 0..7 of parent 0
+    assert (sel["coarse"] == 0).all()
+
+
+# --------------------------------------------------------------- forward ---
+
+@pytest.mark.parametrize("n,B,K,Le", [(256, 4, 2, None), (1024, 16, 4, None), (512, 2, 3, 3), (4096, 16, 3, 1)])
+def test_forward_equals_dense_mask_brute_force(n, B, K, Le):
+    d = 8
+    x = rng_inputs(n, d, seed=31)
+    L = oracle.num_levels(n, B)
+    Le = L if Le is None else Le
+    scale = 1.0 / math.sqrt(d)
+    res = oracle.run(x["q"], x["k"], x["v"], B=B, K=K, Le=Le, backward=False)
+    s = res["slices"][0]
+    o_ref, lse_ref, width = dense_masked(x["q"][0], x["k"][0], x["v"][0], B, L, Le,
+                                         s["sel"]["levels"][1], s["sel"]["coarse"], scale)
+    kl = oracle.level_topk(n, B, L, K)
+    assert width == kl[1] * B + Le        # per-query key set: K*B fine + L coarse
+    np.testing.assert_allclose(s["o"], o_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(s["lse"], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_full_selection_is_dense_attention_plus_enrichment():
+    n, B, d = 1024, 16, 16
+    x = rng_inputs(n, d, seed=41)
+    L = oracle.num_levels(n, B)
+    scale = 1.0 / math.sqrt(d)
+    res = oracle.run(x["q"], x["k"], x["v"], B=B, K=64, backward=False)
+    s = res["slices"][0]
+    q, k, v = (torch.tensor(x[a][0], dtype=torch.float64) for a in ("q", "k", "v"))
+    coarse = torch.tensor(s["sel"]["coarse"][:, 0]).long()
+    kc = k.reshape(-1, B, d).mean(1)[coarse]            # [T, d]: the block's coarse token
+    vc = v.reshape(-1, B, d).mean(1)[coarse]
+    logits = scale * q @ k.T                            # [n, n]
+    lc = scale * (q.reshape(-1, B, d) * kc[:, None, :]).sum(-1).reshape(n, 1) + math.log(B)
+    z = torch.cat([logits, lc], 1)
+    lse = torch.logsumexp(z, 1)
+    p = torch.exp(z - lse[:, None])
+    o = p[:, :n] @ v + p[:, n:] * vc.repeat_interleave(B, 0)
+    np.testing.assert_allclose(s["o"], o.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(s["lse"], lse.numpy(), rtol=1e-12)
+
+
+def test_no_enrichment_full_selection_is_textbook_attention():
+    n, B, d = 1024, 16, 16
+    x = rng_inputs(n, d, seed=42)
+    res = oracle.run(x["q"], x["k"], x["v"], B=B, K=64, Le=0, backward=False)
+    q, k, v = (torch.tensor(x[a][0], dtype=torch.float64)[None, None] for a in ("q", "k", "v"))
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v)[0, 0]
+    np.testing.assert_allclose(res["o"][0], o.numpy(), rtol=1e-10, atol=1e-12)
+    lse = torch.logsumexp((q[0, 0] @ k[0, 0].T) / math.sqrt(d), 1)
+    np.testing.assert_allclose(res["lse"][0], lse.numpy(), rtol=1e-12)
+
+
+def test_fwd_row_subset_matches_full():
+    n, B, K, d = 4096, 16, 4, 8
+    x = rng_inputs(n, d, seed=43)
+    res = oracle.run(x["q"], x["k"], x["v"], B=B, K=K, backward=False)
+    s = res["slices"][0]
+    rows = np.array([0, 5, 17, 1000, 4095])
+    o, lse = oracle.fwd(x["q"][0], x["k"][0], x["v"][0], s["kpyr"], s["vpyr"], B, res["L"], res["Le"],
+                        s["sel"]["levels"][1], s["sel"]["coarse"], res["scale"], qlist=rows)
+    np.testing.assert_array_equal(o, s["o"][rows])
+    np.testing.assert_array_equal(lse, s["lse"][rows])
+
+
+# ------------------------------------------------------------- transpose ---
+
+def test_transpose_matches_dense_boolean_matrix():
+    rng = np.random.default_rng(3)
+    T, K = 300, 7
+    sel = np.stack([np.sort(rng.choice(T, K, replace=False)) for _ in range(T)]).astype(np.int32)
+    col_ptr, row_idx = oracle.transpose(sel, T)
+    M = np.zeros((T, T), bool)
+    M[np.repeat(np.arange(T), K), sel.ravel()] = True
+    cols, rows = np.nonzero(M.T)          # row-major over M^T: ascending rows per column
+    assert col_ptr[-1] == T * K
+    np.testing.assert_array_equal(np.diff(col_ptr), M.sum(0))
+    np.testing.assert_array_equal(row_idx, rows)
+    np.testing.assert_array_equal(np.repeat(np.arange(T), np.diff(col_ptr)), cols)
+    # round trip back to CSR reproduces the sorted rows
+    back = [[] for _ in range(T)]
+    for j in range(T):
+        for i in row_idx[col_ptr[j]:col_ptr[j + 1]]:
+            back[i].append(j)
+    np.testing.assert_array_equal(np.array(back), sel)
+
+
+# -------------------------------------------------------------- backward ---
+
+def _loss(q, k, v, dout, B, L, Le, sel, coarse, scale):
+    kp, vp = oracle.pool(k, B, L), oracle.pool(v, B, L)
+    o, _ = oracle.fwd(q, k, v, kp, vp, B, L, Le, sel, coarse, scale)
+    return float((o * dout.astype(np.float64)).sum())
+
+
+def test_backward_central_finite_differences():
+    n, B, K, d = 64, 4, 2, 8
+    L = oracle.num_levels(n, B)
+    x = rng_inputs(n, d, seed=51)
+    q, k, v, do = (x[a][0] for a in ("q", "k", "v", "dout"))
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=K)
+    s = res["slices"][0]
+    sel, coarse, scale = s["sel"]["levels"][1], s["sel"]["coarse"], res["scale"]
+    grads = {"q": s["dq"], "k": s["dk"], "v": s["dv"]}
+    h = 2.0 ** -10
+    rng = np.random.default_rng(0)
+    for name in ("q", "k", "v"):
+        for _ in range(25):
+            t, c = int(rng.integers(n)), int(rng.integers(d))
+            args = {"q": q.copy(), "k": k.copy(), "v": v.copy()}
+            args[name][t, c] += h
+            lp = _loss(args["q"], args["k"], args["v"], do, B, L, L, sel, coarse, scale)
+            args[name][t, c] -= 2 * h
+            lm = _loss(args["q"], args["k"], args["v"], do, B, L, L, sel, coarse, scale)
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - grads[name][t, c]) <= 1e-5 * max(1.0, abs(fd)), (name, t, c, fd, grads[name][t, c])
+
+
+def _torch_masked_grads(x, B, L, Le, sel, coarse, scale):
+    """Autograd of the dense-mask formulation; pooled K, V are torch means of
+    the fine rows, so their gradient reaches the fine rows through autograd."""
+    q, k, v, do = (torch.tensor(x[a][0], dtype=torch.float64, requires_grad=(a != "dout"))
+                   for a in ("q", "k", "v", "dout"))
+    n, d = q.shape
+    keys, vals = [k], [v]
+    for l in range(1, Le + 1):
+        keys.append(k.reshape(n // B ** l, B ** l, d).mean(1))
+        vals.append(v.reshape(n // B ** l, B ** l, d).mean(1))
+    K_all, V_all = torch.cat(keys), torch.cat(vals)
+    mask = torch.full((n, K_all.shape[0]), -math.inf, dtype=torch.float64)
+    col0 = np.cumsum([0] + [a.shape[0] for a in keys])
+    for t in range(n):
+        i = t // B
+        for j in sel[i]:
+            mask[t, j * B:(j + 1) * B] = 0.0
+        for l in range(1, Le + 1):
+            mask[t, col0[l] + coarse[i, l - 1]] = l * math.log(B)
+    z = scale * q @ K_all.T + mask
+    o = torch.softmax(z, 1) @ V_all
+    (o * do).sum().backward()
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+@pytest.mark.parametrize("n,B,K,Le", [(256, 4, 2, None), (1024, 16, 3, None), (512, 2, 2, 2), (4096, 16, 2, 1)])
+def test_backward_equals_autograd_of_dense_mask(n, B, K, Le):
+    d = 8
+    x = rng_inputs(n, d, seed=61)
+    L = oracle.num_levels(n, B)
+    Le = L if Le is None else Le
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=K, Le=Le)
+    s = res["slices"][0]
+    gq, gk, gv = _torch_masked_grads(x, B, L, Le, s["sel"]["levels"][1], s["sel"]["coarse"], res["scale"])
+    np.testing.assert_allclose(s["dq"], gq, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s["dk"], gk, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s["dv"], gv, rtol=1e-9, atol=1e-11)
+
+
+def test_backward_full_no_enrichment_is_textbook():
+    n, B, d = 1024, 16, 16
+    x = rng_inputs(n, d, seed=71)
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=64, Le=0)
+    q, k, v = (torch.tensor(x[a][0], dtype=torch.float64, requires_grad=True)[None, None] for a in ("q", "k", "v"))
+    for t in (q, k, v):
+        t.retain_grad()
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v)
+    (o[0, 0] * torch.tensor(x["dout"][0], dtype=torch.float64)).sum().backward()
+    np.testing.assert_allclose(res["dq"][0], q.grad[0, 0].numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(res["dk"][0], k.grad[0, 0].numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(res["dv"][0], v.grad[0, 0].numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_backward_sampled_rows_and_blocks_match_full():
+    n, B, K, d = 4096, 16, 4, 8
+    x = rng_inputs(n, d, seed=81)
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=K)
+    s = res["slices"][0]
+    L, Le, sc = res["L"], res["Le"], res["scale"]
+    sel, coarse = s["sel"]["levels"][1], s["sel"]["coarse"]
+    rows = np.array([3, 77, 2048, 4095])
+    dq = oracle.bwd_dq_rows(x["q"][0], x["k"][0], x["v"][0], s["kpyr"], s["vpyr"], s["o"][rows], s["lse"][rows],
+                            x["dout"][0], B, L, Le, sel, coarse, sc, rows)
+    np.testing.assert_allclose(dq, s["dq"][rows], rtol=1e-12, atol=1e-14)
+    blocks = np.unique(np.concatenate([sel[0], coarse[:3, 0], [0, 255]]))
+    dk, dv = oracle.bwd_dkv_blocks(x["q"][0], x["k"][0], x["v"][0], s["kpyr"], s["vpyr"], s["o"], s["lse"],
+                                   x["dout"][0], B, L, Le, sel, coarse, sc, blocks)
+    tok = (blocks[:, None] * B + np.arange(B)[None]).ravel()
+    np.testing.assert_allclose(dk, s["dk"][tok], rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dv, s["dv"][tok], rtol=1e-10, atol=1e-13)
+
+
+# ------------------------------------------------------------- generator ---
+
+def test_splitmix64_published_vector():
+    g = json.load(open(os.path.join(GOLDEN, "splitmix64_seed1234567.json")))
+    got = synth.uint64_stream(g["state"], 0, len(g["outputs"]))
+    assert [int(a) for a in got] == [int(b) for b in g["outputs"]]
+
+
+def test_generator_moments_and_bf16():
+    z = synth.normal(synth.stream_key(1, 0, 0), 200000)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+    r = synth.bf16_round(np.array([1.0, 1.00390625, 1.01171875, -3.1415926], np.float32))
+    assert r[0] == 1.0 and r[1] == 1.0 and r[2] == 1.015625   # ties to even
+    assert (r.view(np.uint32) & 0xFFFF).max() == 0
