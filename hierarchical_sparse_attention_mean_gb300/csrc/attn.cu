@@ -1,0 +1,33 @@
+// attn.cu -- picks the kernels of the forward and backward attention passes
+// and sets up their arguments.
+#include "attn.h"
+
+namespace llsa {
+
+int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, const float* pyr,
+               const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, cudaStream_t st) {
+    AttnArgs a = make_attn_args(s);
+    a.q = q; a.k = k; a.v = v;
+    a.kpyr = pyr + s.slices * a.pyr_stride;
+    a.vpyr = pyr + 2 * s.slices * a.pyr_stride;
+    a.sel = sel_idx; a.coarse = coarse_idx; a.out_o = o; a.lse = lse;
+    return launch_fwd_simt(s, a, st);
+}
+
+int launch_bwd(const Shape& s, const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, const float* pyr, const int32_t* sel_idx, const int32_t* coarse_idx,
+               const int32_t* col_ptr, const int32_t* row_idx, void* dq, void* dk, void* dv, void* ws,
+               cudaStream_t st) {
+    AttnArgs a = make_attn_args(s);
+    a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse_in = lse;
+    a.kpyr = pyr + s.slices * a.pyr_stride;
+    a.vpyr = pyr + 2 * s.slices * a.pyr_stride;
+    a.sel = sel_idx; a.coarse = coarse_idx; a.col_ptr = col_ptr; a.row_idx = row_idx;
+    a.dq = dq; a.dk = dk; a.dv = dv;
+    carve_bwd_workspace(s, ws, &a);
+    LLSA_TRY(launch_bwd_dq_simt(s, a, st));
+    LLSA_TRY(launch_coarse_reduce(s, a, st));
+    return launch_bwd_dkv_simt(s, a, st);
+}
+
+}  // namespace llsa

@@ -1,0 +1,54 @@
+// attn.h -- arguments and helpers shared by the attention kernels (CUDA-core
+// path and tensor-core path).
+#pragma once
+
+#include "internal.h"
+
+namespace llsa {
+
+struct AttnArgs {
+    const void *q, *k, *v, *o, *dout;
+    const float *kpyr, *vpyr;  // K and V pyramids of slice 0
+    long long pyr_stride;      // floats per slice pyramid (P * d)
+    const int *sel, *coarse, *col_ptr, *row_idx;
+    void* out_o;
+    float* lse;
+    const float* lse_in;
+    void *dq, *dk, *dv;
+    float *Dbuf, *gK, *gV, *dKc, *dVc;  // backward workspace
+    long long slices;
+    int n, d, B, L, Le, K1, T, P;
+    float scale, lnB;
+    LevelTable lv;
+    int* status;
+};
+
+AttnArgs make_attn_args(const Shape& s);
+size_t align256(size_t x);
+void carve_bwd_workspace(const Shape& s, void* ws, AttnArgs* a);
+
+int launch_fwd_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
+int launch_bwd_dq_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
+int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st);
+int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
+
+// Adds to the fine-key gradients of column chunk c4 of key block j the
+// gradients of the pooled tokens above it: the level-l ancestor of block j is
+// j / B^(l-1); each of its B^l fine rows receives 1/B^l of its gradient.
+__device__ __forceinline__ void add_pooled_grads(const AttnArgs& a, long long slice, int j, int c4, float* kk,
+                                                 float* vv) {
+    long long span = a.B;
+    int anc = j;
+    for (int l = 1; l <= a.Le; l++) {
+        const long long off = (slice * a.P + a.lv.row_offset[l] + anc) * (long long)a.d + c4 * 4;
+        const float4 gk = *reinterpret_cast<const float4*>(a.dKc + off);
+        const float4 gv = *reinterpret_cast<const float4*>(a.dVc + off);
+        const float inv = 1.0f / (float)span;
+        kk[0] += gk.x * inv; kk[1] += gk.y * inv; kk[2] += gk.z * inv; kk[3] += gk.w * inv;
+        vv[0] += gv.x * inv; vv[1] += gv.y * inv; vv[2] += gv.z * inv; vv[3] += gv.w * inv;
+        span *= a.B;
+        anc /= a.B;
+    }
+}
+
+}  // namespace llsa

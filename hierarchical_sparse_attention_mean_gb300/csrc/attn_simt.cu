@@ -1,0 +1,563 @@
+// attn_simt.cu -- block-sparse attention with KV enrichment, forward and
+// backward, on the CUDA cores (fp32 arithmetic). This is the fp32 path and the
+// general-shape path (any B, any d multiple of 8 up to 256).
+//
+// Method: Pith review of arXiv 2512.16615. "Core claim": each query block
+// attends the B tokens of each of its K selected fine blocks plus one coarse
+// K/V token per level, reweighted by W^(l) = B^l (KV Reweighting, referee
+// minor comment 2: read as + ln B^l on the logit). "What carries the
+// argument" and the referee's Sec. 4.3 / Figure 4 comments: the backward uses
+// only sparse indices; dK/dV run key-major over the CSC from the index
+// transpose; gradients of the pooled (coarse) keys and values return to the
+// fine rows they average, 1/B^l each.
+//
+// Kernels:
+//   fwd_simt       one CTA per query block: scores in shared memory, softmax,
+//                  P V; writes o and lse.
+//   bwd_dq_simt    one CTA per query block: D = rowsum(dO o), P, dS, dq, and
+//                  the per-(query block, level) coarse partial gradients.
+//   coarse_reduce  one CTA per pooled token used by enrichment: deterministic
+//                  sum of the coarse partials of the query blocks that used it.
+//   bwd_dkv_simt   one CTA per fine key block: walks its CSC column (query
+//                  blocks ascending), accumulates dk, dv; adds the pooled-level
+//                  gradients through the means.
+#include <string.h>
+
+#include "attn.h"
+
+namespace llsa {
+namespace {
+
+constexpr int kTileKeys = 64;
+constexpr int kMaxItems = 4;  // float4 outputs per thread
+
+__device__ __forceinline__ float dot_smem(const float* a, const float* b, int d) {
+    float acc = 0.f;
+    for (int c = 0; c < d; c += 4) {
+        float4 x = *reinterpret_cast<const float4*>(a + c);
+        float4 y = *reinterpret_cast<const float4*>(b + c);
+        acc = fmaf(x.x, y.x, acc); acc = fmaf(x.y, y.y, acc);
+        acc = fmaf(x.z, y.z, acc); acc = fmaf(x.w, y.w, acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ float dot_smem_global(const float* a, const float* g, int d) {
+    float acc = 0.f;
+    for (int c = 0; c < d; c += 4) {
+        float4 x = *reinterpret_cast<const float4*>(a + c);
+        float4 y = __ldg(reinterpret_cast<const float4*>(g + c));
+        acc = fmaf(x.x, y.x, acc); acc = fmaf(x.y, y.y, acc);
+        acc = fmaf(x.z, y.z, acc); acc = fmaf(x.w, y.w, acc);
+    }
+    return acc;
+}
+
+// rows x d tensor rows -> fp32 shared memory with row stride ds
+template <typename T>
+__device__ __forceinline__ void rows_to_smem(float* dst, int ds, const T* src, int rows, int d) {
+    const int V = d / 8;
+    for (int it = threadIdx.x; it < rows * V; it += blockDim.x) {
+        const int r = it / V, c8 = it % V;
+        float f[8];
+        load8(src + (long long)r * d + c8 * 8, f);
+        float4* p = reinterpret_cast<float4*>(dst + r * ds + c8 * 8);
+        p[0] = make_float4(f[0], f[1], f[2], f[3]);
+        p[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+}
+
+// gathered key rows (token list) -> fp32 shared memory
+template <typename T>
+__device__ __forceinline__ void gather_to_smem(float* dst, int ds, const T* base, const int* tok, int rows, int d) {
+    const int V = d / 8;
+    for (int it = threadIdx.x; it < rows * V; it += blockDim.x) {
+        const int r = it / V, c8 = it % V;
+        float f[8];
+        load8(base + (long long)tok[r] * d + c8 * 8, f);
+        float4* p = reinterpret_cast<float4*>(dst + r * ds + c8 * 8);
+        p[0] = make_float4(f[0], f[1], f[2], f[3]);
+        p[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+}
+
+__device__ __forceinline__ int checked(int v, int lim, int* status) {
+    if (v < 0 || v >= lim) {
+        set_status(status, LLSA_ERR_BAD_INDEX);
+        return 0;
+    }
+    return v;
+}
+
+// token numbers of the K1 * B fine keys of query block i
+__device__ __forceinline__ void key_tokens(const AttnArgs& a, long long slice, int i, int* keytok) {
+    const int* srow = a.sel + (slice * a.T + i) * a.K1;
+    for (int kk = threadIdx.x; kk < a.K1 * a.B; kk += blockDim.x)
+        keytok[kk] = checked(srow[kk / a.B], a.T, a.status) * a.B + kk % a.B;
+}
+
+__device__ __forceinline__ const float* coarse_row(const AttnArgs& a, const float* pyr, long long slice, int i,
+                                                   int l) {
+    // level l+1 enrichment token of query block i
+    const int e = checked(a.coarse[(slice * a.T + i) * a.L + l], a.lv.n_level[l + 1], a.status);
+    return pyr + slice * a.pyr_stride + (long long)(a.lv.row_offset[l + 1] + e) * a.d;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) fwd_simt_kernel(AttnArgs a) {
+    extern __shared__ float4 sm4[];
+    const int d = a.d, B = a.B, nf = a.K1 * B, NK = nf + a.Le, NKP = NK | 1, ds = d + 4;
+    float* qs = reinterpret_cast<float*>(sm4);
+    float* kv = qs + B * ds;
+    float* S = kv + kTileKeys * ds;
+    int* keytok = reinterpret_cast<int*>(S + B * NKP);
+    const long long slice = blockIdx.y;
+    const int i = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const long long tok0 = slice * a.n + (long long)i * B;
+    const T* kbase = static_cast<const T*>(a.k) + slice * a.n * (long long)d;
+    const T* vbase = static_cast<const T*>(a.v) + slice * a.n * (long long)d;
+
+    key_tokens(a, slice, i, keytok);
+    rows_to_smem(qs, ds, static_cast<const T*>(a.q) + tok0 * d, B, d);
+    __syncthreads();
+    for (int t0 = 0; t0 < nf; t0 += kTileKeys) {
+        const int tn = min(kTileKeys, nf - t0);
+        gather_to_smem(kv, ds, kbase, keytok + t0, tn, d);
+        __syncthreads();
+        const int kk = tid & (kTileKeys - 1);
+        if (kk < tn)
+            for (int r = tid / kTileKeys; r < B; r += nt / kTileKeys)
+                S[r * NKP + t0 + kk] = a.scale * dot_smem(qs + r * ds, kv + kk * ds, d);
+        __syncthreads();
+    }
+    for (int pr = tid; pr < B * a.Le; pr += nt) {
+        const int r = pr / a.Le, l = pr % a.Le;
+        S[r * NKP + nf + l] = a.scale * dot_smem_global(qs + r * ds, coarse_row(a, a.kpyr, slice, i, l), d) +
+                              (float)(l + 1) * a.lnB;
+    }
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int r = warp; r < B; r += nt / 32) {
+        float* sr = S + r * NKP;
+        float m = -INFINITY;
+        for (int c = lane; c < NK; c += 32) m = fmaxf(m, sr[c]);
+        m = warp_max(m);
+        float z = 0.f;
+        for (int c = lane; c < NK; c += 32) z += expf(sr[c] - m);
+        z = warp_sum(z);
+        const float lse = m + logf(z);
+        for (int c = lane; c < NK; c += 32) sr[c] = expf(sr[c] - lse);
+        if (lane == 0) a.lse[tok0 + r] = lse;
+    }
+    __syncthreads();
+    const int C4 = d / 4, items = B * C4;
+    float acc[kMaxItems][4];
+#pragma unroll
+    for (int m = 0; m < kMaxItems; m++)
+#pragma unroll
+        for (int u = 0; u < 4; u++) acc[m][u] = 0.f;
+    for (int t0 = 0; t0 < nf; t0 += kTileKeys) {
+        const int tn = min(kTileKeys, nf - t0);
+        __syncthreads();
+        gather_to_smem(kv, ds, vbase, keytok + t0, tn, d);
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kMaxItems; m++) {
+            const int it = tid + m * nt;
+            if (it < items) {
+                const int r = it / C4, c4 = it % C4;
+                const float* pr = S + r * NKP + t0;
+                for (int kk = 0; kk < tn; kk++) {
+                    const float p = pr[kk];
+                    const float4 v4 = *reinterpret_cast<const float4*>(kv + kk * ds + c4 * 4);
+                    acc[m][0] = fmaf(p, v4.x, acc[m][0]); acc[m][1] = fmaf(p, v4.y, acc[m][1]);
+                    acc[m][2] = fmaf(p, v4.z, acc[m][2]); acc[m][3] = fmaf(p, v4.w, acc[m][3]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kMaxItems; m++) {
+        const int it = tid + m * nt;
+        if (it < items) {
+            const int r = it / C4, c4 = it % C4;
+            for (int l = 0; l < a.Le; l++) {
+                const float p = S[r * NKP + nf + l];
+                const float4 v4 = __ldg(reinterpret_cast<const float4*>(coarse_row(a, a.vpyr, slice, i, l) + c4 * 4));
+                acc[m][0] = fmaf(p, v4.x, acc[m][0]); acc[m][1] = fmaf(p, v4.y, acc[m][1]);
+                acc[m][2] = fmaf(p, v4.z, acc[m][2]); acc[m][3] = fmaf(p, v4.w, acc[m][3]);
+            }
+            store4(static_cast<T*>(a.out_o) + (tok0 + r) * d + c4 * 4, acc[m]);
+        }
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) bwd_dq_simt_kernel(AttnArgs a) {
+    extern __shared__ float4 sm4[];
+    const int d = a.d, B = a.B, nf = a.K1 * B, NK = nf + a.Le, NKP = NK | 1, ds = d + 4;
+    float* qs = reinterpret_cast<float*>(sm4);
+    float* dos = qs + B * ds;
+    float* ks = dos + B * ds;
+    float* vs = ks + kTileKeys * ds;
+    float* P = vs + kTileKeys * ds;
+    float* dS = P + B * NKP;
+    float* lse_s = dS + B * NKP;
+    float* D_s = lse_s + B;
+    int* keytok = reinterpret_cast<int*>(D_s + B);
+    const long long slice = blockIdx.y;
+    const int i = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const long long tok0 = slice * a.n + (long long)i * B;
+    const T* kbase = static_cast<const T*>(a.k) + slice * a.n * (long long)d;
+    const T* vbase = static_cast<const T*>(a.v) + slice * a.n * (long long)d;
+
+    key_tokens(a, slice, i, keytok);
+    rows_to_smem(qs, ds, static_cast<const T*>(a.q) + tok0 * d, B, d);
+    rows_to_smem(dos, ds, static_cast<const T*>(a.dout) + tok0 * d, B, d);
+    __syncthreads();
+    // D_t = dO_t . o_t with o as stored by the forward
+    for (int r = warp; r < B; r += nt / 32) {
+        const T* orow = static_cast<const T*>(a.o) + (tok0 + r) * d;
+        float acc = 0.f;
+        for (int c = lane * 8; c < d; c += 256) {
+            float f[8];
+            load8(orow + c, f);
+#pragma unroll
+            for (int u = 0; u < 8; u++) acc = fmaf(dos[r * ds + c + u], f[u], acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) {
+            D_s[r] = acc;
+            a.Dbuf[tok0 + r] = acc;
+            lse_s[r] = a.lse_in[tok0 + r];
+        }
+    }
+    __syncthreads();
+    for (int t0 = 0; t0 < nf; t0 += kTileKeys) {
+        const int tn = min(kTileKeys, nf - t0);
+        gather_to_smem(ks, ds, kbase, keytok + t0, tn, d);
+        gather_to_smem(vs, ds, vbase, keytok + t0, tn, d);
+        __syncthreads();
+        const int kk = tid & (kTileKeys - 1);
+        if (kk < tn)
+            for (int r = tid / kTileKeys; r < B; r += nt / kTileKeys) {
+                const float s = a.scale * dot_smem(qs + r * ds, ks + kk * ds, d);
+                const float p = expf(s - lse_s[r]);
+                const float dp = dot_smem(dos + r * ds, vs + kk * ds, d);
+                P[r * NKP + t0 + kk] = p;
+                dS[r * NKP + t0 + kk] = p * (dp - D_s[r]);
+            }
+        __syncthreads();
+    }
+    for (int pr = tid; pr < B * a.Le; pr += nt) {
+        const int r = pr / a.Le, l = pr % a.Le;
+        const float s = a.scale * dot_smem_global(qs + r * ds, coarse_row(a, a.kpyr, slice, i, l), d) +
+                        (float)(l + 1) * a.lnB;
+        const float p = expf(s - lse_s[r]);
+        const float dp = dot_smem_global(dos + r * ds, coarse_row(a, a.vpyr, slice, i, l), d);
+        P[r * NKP + nf + l] = p;
+        dS[r * NKP + nf + l] = p * (dp - D_s[r]);
+    }
+    __syncthreads();
+    // dq = scale * sum_x dS_x k_x
+    const int C4 = d / 4, items = B * C4;
+    float acc[kMaxItems][4];
+#pragma unroll
+    for (int m = 0; m < kMaxItems; m++)
+#pragma unroll
+        for (int u = 0; u < 4; u++) acc[m][u] = 0.f;
+    for (int t0 = 0; t0 < nf; t0 += kTileKeys) {
+        const int tn = min(kTileKeys, nf - t0);
+        __syncthreads();
+        gather_to_smem(ks, ds, kbase, keytok + t0, tn, d);
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kMaxItems; m++) {
+            const int it = tid + m * nt;
+            if (it < items) {
+                const int r = it / C4, c4 = it % C4;
+                const float* pr = dS + r * NKP + t0;
+                for (int kk = 0; kk < tn; kk++) {
+                    const float g = pr[kk];
+                    const float4 k4 = *reinterpret_cast<const float4*>(ks + kk * ds + c4 * 4);
+                    acc[m][0] = fmaf(g, k4.x, acc[m][0]); acc[m][1] = fmaf(g, k4.y, acc[m][1]);
+                    acc[m][2] = fmaf(g, k4.z, acc[m][2]); acc[m][3] = fmaf(g, k4.w, acc[m][3]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kMaxItems; m++) {
+        const int it = tid + m * nt;
+        if (it < items) {
+            const int r = it / C4, c4 = it % C4;
+            for (int l = 0; l < a.Le; l++) {
+                const float g = dS[r * NKP + nf + l];
+                const float4 k4 = __ldg(reinterpret_cast<const float4*>(coarse_row(a, a.kpyr, slice, i, l) + c4 * 4));
+                acc[m][0] = fmaf(g, k4.x, acc[m][0]); acc[m][1] = fmaf(g, k4.y, acc[m][1]);
+                acc[m][2] = fmaf(g, k4.z, acc[m][2]); acc[m][3] = fmaf(g, k4.w, acc[m][3]);
+            }
+            float out[4] = {a.scale * acc[m][0], a.scale * acc[m][1], a.scale * acc[m][2], a.scale * acc[m][3]};
+            store4(static_cast<T*>(a.dq) + (tok0 + r) * d + c4 * 4, out);
+        }
+    }
+    // coarse partials of this query block: gK = scale sum_t dS_t q_t,
+    // gV = sum_t P_t dO_t, per enrichment level
+    for (int it = tid; it < a.Le * C4; it += nt) {
+        const int l = it / C4, c4 = it % C4;
+        float gk[4] = {0.f, 0.f, 0.f, 0.f}, gv[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = 0; r < B; r++) {
+            const float g = dS[r * NKP + nf + l], p = P[r * NKP + nf + l];
+            const float4 q4 = *reinterpret_cast<const float4*>(qs + r * ds + c4 * 4);
+            const float4 o4 = *reinterpret_cast<const float4*>(dos + r * ds + c4 * 4);
+            gk[0] = fmaf(g, q4.x, gk[0]); gk[1] = fmaf(g, q4.y, gk[1]);
+            gk[2] = fmaf(g, q4.z, gk[2]); gk[3] = fmaf(g, q4.w, gk[3]);
+            gv[0] = fmaf(p, o4.x, gv[0]); gv[1] = fmaf(p, o4.y, gv[1]);
+            gv[2] = fmaf(p, o4.z, gv[2]); gv[3] = fmaf(p, o4.w, gv[3]);
+        }
+        const long long off = ((slice * a.T + i) * a.Le + l) * (long long)d + c4 * 4;
+        *reinterpret_cast<float4*>(a.gK + off) =
+            make_float4(a.scale * gk[0], a.scale * gk[1], a.scale * gk[2], a.scale * gk[3]);
+        *reinterpret_cast<float4*>(a.gV + off) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+    }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(512) bwd_dkv_simt_kernel(AttnArgs a) {
+    extern __shared__ float4 sm4[];
+    const int d = a.d, B = a.B, ds = d + 4, BP = B + 1;
+    float* ks = reinterpret_cast<float*>(sm4);
+    float* vs = ks + B * ds;
+    float* qs = vs + B * ds;
+    float* dos = qs + B * ds;
+    float* Pm = dos + B * ds;
+    float* dSm = Pm + B * BP;
+    float* lse_s = dSm + B * BP;
+    float* D_s = lse_s + B;
+    const long long slice = blockIdx.y;
+    const int j = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+    const long long key0 = slice * a.n + (long long)j * B;
+    rows_to_smem(ks, ds, static_cast<const T*>(a.k) + key0 * d, B, d);
+    rows_to_smem(vs, ds, static_cast<const T*>(a.v) + key0 * d, B, d);
+    const int C4 = d / 4, items = B * C4;
+    float ak[kMaxItems][4], av[kMaxItems][4];
+#pragma unroll
+    for (int m = 0; m < kMaxItems; m++)
+#pragma unroll
+        for (int u = 0; u < 4; u++) { ak[m][u] = 0.f; av[m][u] = 0.f; }
+    const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
+    const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
+    const int beg = cp[j], end = cp[j + 1];
+    for (int x = beg; x < end; x++) {
+        const int i = checked(ri[x], a.T, a.status);
+        const long long tok0 = slice * a.n + (long long)i * B;
+        __syncthreads();
+        rows_to_smem(qs, ds, static_cast<const T*>(a.q) + tok0 * d, B, d);
+        rows_to_smem(dos, ds, static_cast<const T*>(a.dout) + tok0 * d, B, d);
+        for (int r = tid; r < B; r += nt) {
+            lse_s[r] = a.lse_in[tok0 + r];
+            D_s[r] = a.Dbuf[tok0 + r];
+        }
+        __syncthreads();
+        for (int pr = tid; pr < B * B; pr += nt) {
+            const int r = pr / B, c = pr % B;
+            const float s = a.scale * dot_smem(qs + r * ds, ks + c * ds, d);
+            const float p = expf(s - lse_s[r]);
+            const float dp = dot_smem(dos + r * ds, vs + c * ds, d);
+            Pm[r * BP + c] = p;
+            dSm[r * BP + c] = p * (dp - D_s[r]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kMaxItems; m++) {
+            const int it = tid + m * nt;
+            if (it < items) {
+                const int c = it / C4, c4 = it % C4;
+                for (int r = 0; r < B; r++) {
+                    const float p = Pm[r * BP + c], g = dSm[r * BP + c];
+                    const float4 q4 = *reinterpret_cast<const float4*>(qs + r * ds + c4 * 4);
+                    const float4 o4 = *reinterpret_cast<const float4*>(dos + r * ds + c4 * 4);
+                    av[m][0] = fmaf(p, o4.x, av[m][0]); av[m][1] = fmaf(p, o4.y, av[m][1]);
+                    av[m][2] = fmaf(p, o4.z, av[m][2]); av[m][3] = fmaf(p, o4.w, av[m][3]);
+                    ak[m][0] = fmaf(g, q4.x, ak[m][0]); ak[m][1] = fmaf(g, q4.y, ak[m][1]);
+                    ak[m][2] = fmaf(g, q4.z, ak[m][2]); ak[m][3] = fmaf(g, q4.w, ak[m][3]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kMaxItems; m++) {
+        const int it = tid + m * nt;
+        if (it < items) {
+            const int c = it / C4, c4 = it % C4;
+            float kk[4], vv[4];
+            for (int u = 0; u < 4; u++) { kk[u] = a.scale * ak[m][u]; vv[u] = av[m][u]; }
+            add_pooled_grads(a, slice, j, c4, kk, vv);
+            store4(static_cast<T*>(a.dk) + (key0 + c) * d + c4 * 4, kk);
+            store4(static_cast<T*>(a.dv) + (key0 + c) * d + c4 * 4, vv);
+        }
+    }
+}
+
+int attn_threads(int B, int d) {
+    int items = B * d / 4, nt = 128;
+    while (nt < 512 && items > kMaxItems * nt) nt *= 2;
+    return items > kMaxItems * nt ? -1 : nt;
+}
+
+template <typename K>
+void allow_smem(K kernel, size_t smem) {
+    if (smem > 48 * 1024) cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+}  // namespace
+
+// Gradient of every pooled token used by enrichment: the sum, in ascending
+// query-block order, of the coarse partials of the query blocks that used it.
+// Level 1 tokens are fine blocks that their users also selected (TOP1 picks
+// from the selection), so the fine CSC column lists the candidates; level
+// l >= 2 tokens scan the level's ancestors (one rank-1 token per ancestor).
+__global__ void __launch_bounds__(64) coarse_reduce_kernel(AttnArgs a) {
+    const long long slice = blockIdx.y;
+    const int row = blockIdx.x;  // pyramid row over levels 1..Le
+    int l = 1;
+    while (l < a.Le && row >= a.lv.row_offset[l + 1]) l++;
+    const int e = row - a.lv.row_offset[l];
+    const int d = a.d, C4 = d / 4, tid = threadIdx.x, lane = tid & 31;
+    const bool active = tid < C4;
+    float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
+    auto add = [&](int i) {
+        if (!active) return;
+        const long long off = ((slice * a.T + i) * a.Le + (l - 1)) * (long long)d + tid * 4;
+        const float4 k4 = *reinterpret_cast<const float4*>(a.gK + off);
+        const float4 v4 = *reinterpret_cast<const float4*>(a.gV + off);
+        ak.x += k4.x; ak.y += k4.y; ak.z += k4.z; ak.w += k4.w;
+        av.x += v4.x; av.y += v4.y; av.z += v4.z; av.w += v4.w;
+    };
+    if (l == 1) {
+        const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
+        const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
+        for (int x = cp[e]; x < cp[e + 1]; x++) {
+            const int i = ri[x];
+            if (i >= 0 && i < a.T && a.coarse[(slice * a.T + i) * a.L] == e) add(i);
+        }
+    } else {
+        int span = 1;
+        for (int u = 1; u < l; u++) span *= a.B;
+        const int nl = a.lv.n_level[l];
+        for (int a0 = 0; a0 < nl; a0 += 32) {
+            const int anc = a0 + lane;
+            const bool hit = anc < nl && a.coarse[(slice * a.T + (long long)anc * span) * a.L + (l - 1)] == e;
+            unsigned bits = __ballot_sync(0xffffffffu, hit);
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1;
+                const int first = (a0 + b) * span;
+                for (int i = first; i < first + span; i++) add(i);
+            }
+        }
+    }
+    if (active) {
+        const long long off = (slice * a.P + a.lv.row_offset[l] + e) * (long long)d + tid * 4;
+        *reinterpret_cast<float4*>(a.dKc + off) = ak;
+        *reinterpret_cast<float4*>(a.dVc + off) = av;
+    }
+}
+
+AttnArgs make_attn_args(const Shape& s) {
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.pyr_stride = (long long)s.P * s.d;
+    a.slices = s.slices;
+    a.n = s.n; a.d = s.d; a.B = s.B; a.L = s.L; a.Le = s.Le; a.K1 = s.K1; a.T = s.T; a.P = s.P;
+    a.scale = s.scale;
+    a.lnB = logf((float)s.B);
+    a.lv = level_table(s);
+    a.status = status_ptr();
+    return a;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+size_t bwd_workspace_bytes(const Shape& s) {
+    size_t b = align256(sizeof(float) * s.slices * (size_t)s.n);                       // D
+    b += 2 * align256(sizeof(float) * s.slices * (size_t)s.T * s.Le * s.d);            // gK, gV
+    b += 2 * align256(sizeof(float) * s.slices * (size_t)s.P * s.d);                   // dKc, dVc
+    return b;
+}
+
+void carve_bwd_workspace(const Shape& s, void* ws, AttnArgs* a) {
+    char* w = static_cast<char*>(ws);
+    a->Dbuf = reinterpret_cast<float*>(w);
+    w += align256(sizeof(float) * s.slices * (size_t)s.n);
+    const size_t gsz = align256(sizeof(float) * s.slices * (size_t)s.T * s.Le * s.d);
+    a->gK = reinterpret_cast<float*>(w); w += gsz;
+    a->gV = reinterpret_cast<float*>(w); w += gsz;
+    const size_t csz = align256(sizeof(float) * s.slices * (size_t)s.P * s.d);
+    a->dKc = reinterpret_cast<float*>(w); w += csz;
+    a->dVc = reinterpret_cast<float*>(w);
+}
+
+int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st) {
+    if (s.Le == 0) return LLSA_OK;
+    int rows = 0;
+    for (int l = 1; l <= s.Le; l++) rows += s.n_level[l];
+    LLSA_LAUNCH("coarse_reduce", st, coarse_reduce_kernel<<<dim3(rows, (unsigned)s.slices), 64, 0, st>>>(a));
+    return LLSA_OK;
+}
+
+int launch_fwd_simt(const Shape& s, const AttnArgs& a, cudaStream_t st) {
+    const int nt = attn_threads(s.B, s.d);
+    if (nt < 0 || s.slices > 65535) return LLSA_ERR_UNSUPPORTED;
+    const int ds = s.d + 4, NKP = (s.K1 * s.B + s.Le) | 1;
+    const size_t smem = sizeof(float) * ((size_t)s.B * ds + kTileKeys * ds + (size_t)s.B * NKP) +
+                        sizeof(int) * (size_t)s.K1 * s.B;
+    if (smem > 220 * 1024) return LLSA_ERR_UNSUPPORTED;
+    dim3 grid(s.T, (unsigned)s.slices);
+    if (s.dtype == LLSA_DTYPE_BF16) {
+        allow_smem(fwd_simt_kernel<__nv_bfloat16>, smem);
+        LLSA_LAUNCH("fwd_simt", st, fwd_simt_kernel<__nv_bfloat16><<<grid, nt, smem, st>>>(a));
+    } else {
+        allow_smem(fwd_simt_kernel<float>, smem);
+        LLSA_LAUNCH("fwd_simt", st, fwd_simt_kernel<float><<<grid, nt, smem, st>>>(a));
+    }
+    return LLSA_OK;
+}
+
+int launch_bwd_dq_simt(const Shape& s, const AttnArgs& a, cudaStream_t st) {
+    const int nt = attn_threads(s.B, s.d);
+    if (nt < 0 || s.slices > 65535) return LLSA_ERR_UNSUPPORTED;
+    const int ds = s.d + 4, NKP = (s.K1 * s.B + s.Le) | 1;
+    const size_t smem = sizeof(float) * (2 * (size_t)s.B * ds + 2 * kTileKeys * ds + 2 * (size_t)s.B * NKP +
+                                         2 * (size_t)s.B) + sizeof(int) * (size_t)s.K1 * s.B;
+    if (smem > 220 * 1024) return LLSA_ERR_UNSUPPORTED;
+    dim3 grid(s.T, (unsigned)s.slices);
+    if (s.dtype == LLSA_DTYPE_BF16) {
+        allow_smem(bwd_dq_simt_kernel<__nv_bfloat16>, smem);
+        LLSA_LAUNCH("bwd_dq_simt", st, bwd_dq_simt_kernel<__nv_bfloat16><<<grid, nt, smem, st>>>(a));
+    } else {
+        allow_smem(bwd_dq_simt_kernel<float>, smem);
+        LLSA_LAUNCH("bwd_dq_simt", st, bwd_dq_simt_kernel<float><<<grid, nt, smem, st>>>(a));
+    }
+    return LLSA_OK;
+}
+
+int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st) {
+    const int nt = attn_threads(s.B, s.d);
+    if (nt < 0 || s.slices > 65535) return LLSA_ERR_UNSUPPORTED;
+    const int ds = s.d + 4;
+    const size_t smem = sizeof(float) * (4 * (size_t)s.B * ds + 2 * (size_t)s.B * (s.B + 1) + 2 * (size_t)s.B);
+    if (smem > 220 * 1024) return LLSA_ERR_UNSUPPORTED;
+    dim3 grid(s.T, (unsigned)s.slices);
+    if (s.dtype == LLSA_DTYPE_BF16) {
+        allow_smem(bwd_dkv_simt_kernel<__nv_bfloat16>, smem);
+        LLSA_LAUNCH("bwd_dkv_simt", st, bwd_dkv_simt_kernel<__nv_bfloat16><<<grid, nt, smem, st>>>(a));
+    } else {
+        allow_smem(bwd_dkv_simt_kernel<float>, smem);
+        LLSA_LAUNCH("bwd_dkv_simt", st, bwd_dkv_simt_kernel<float><<<grid, nt, smem, st>>>(a));
+    }
+    return LLSA_OK;
+}
+
+}  // namespace llsa

@@ -1,0 +1,254 @@
+// select.cu -- hierarchical Top-K selection and the TOP1 enrichment index.
+//
+// Method: Pith review of arXiv 2512.16615, "Core claim" and "What carries the
+// argument": the coarsest level computes full similarities and keeps the K
+// best per query; each finer level scores only the K*B children of the blocks
+// kept above and carries the indices down (referee comment on Algorithm 1: the
+// parent-to-child map is read as contiguous, children of j are jB..jB+B-1).
+// Scores are raw dot products of pooled Q and K in fp32; ties go to the lower
+// index; stored rows are ascending. The enrichment token of level l for query
+// block i is the rank-1 choice of level l for i's ancestor floor(i / B^(l-1)).
+//
+// One launch per level, coarsest first (each level needs the one above). A CTA
+// owns up to 16 sibling query rows that share one candidate list: candidate
+// key rows are staged through shared memory in tiles (coalesced float4 loads),
+// each warp scores one query row against the tile, and the warp then runs K
+// rounds of a shuffle arg-max tournament over its row's candidates (each lane
+// holding ceil(C/32) of them). K <= 64 and C <= 1024 here, so K tournament
+// rounds cost less than a full bitonic sort of the C candidates.
+#include <limits.h>
+
+#include "internal.h"
+
+namespace llsa {
+namespace {
+
+constexpr int kTile = 64;     // candidate rows per shared-memory tile
+constexpr int kMaxRows = 16;  // query rows (warps) per CTA
+constexpr int kMaxCand = 1024;
+constexpr int kMaxKeep = 64;
+
+struct SelectArgs {
+    const float* qpyr;     // Q pyramid of slice 0 (level rows at row_off)
+    const float* kpyr;     // K pyramid of slice 0
+    long long pyr_stride;  // floats per slice pyramid
+    int row_off;           // first pyramid row of this level
+    int n_l, d, B;
+    const int* parent;     // level l+1 selection of slice 0, or nullptr
+    long long parent_stride;
+    int Kp;
+    int Kl;
+    int* out;
+    long long out_stride;
+    int* coarse;           // [slices][T][L]
+    int T, L, level, span; // span = B^(level-1)
+    int rows_per_cta;
+    int C;                 // candidates per row
+    int n_parent;          // rows of the parent level (index check)
+    int* status;
+};
+
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+    return sa > sb || (sa == sb && ia < ib);
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs a) {
+    extern __shared__ float4 smem4[];
+    const int d = a.d, C = a.C;
+    const int ktile_stride = d + 4;
+    float* ktile = reinterpret_cast<float*>(smem4);                 // [kTile][d+4]
+    float* qrows = ktile + kTile * ktile_stride;                     // [rows][d]
+    float* scores = qrows + kMaxRows * d;                            // [rows][C]
+    int* cand = reinterpret_cast<int*>(scores + kMaxRows * C);       // [C]
+    int* kept = cand + C;                                            // [rows][kMaxKeep]
+
+    const long long slice = blockIdx.y;
+    const int row0 = blockIdx.x * a.rows_per_cta;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nthreads = blockDim.x;
+    const float* qp = a.qpyr + slice * a.pyr_stride + (long long)a.row_off * d;
+    const float* kp = a.kpyr + slice * a.pyr_stride + (long long)a.row_off * d;
+
+    // candidate list (ascending token indices)
+    if (a.parent) {
+        const int* prow = a.parent + slice * a.parent_stride + (long long)(row0 / a.B) * a.Kp;
+        for (int c = threadIdx.x; c < C; c += nthreads) {
+            int j = prow[c / a.B];
+            if (j < 0 || j >= a.n_parent) {
+                set_status(a.status, LLSA_ERR_BAD_INDEX);
+                j = 0;
+            }
+            cand[c] = j * a.B + c % a.B;
+        }
+    } else {
+        for (int c = threadIdx.x; c < C; c += nthreads) cand[c] = c;
+    }
+    // query rows of this CTA
+    const int nrows = min(a.rows_per_cta, a.n_l - row0);
+    for (int i = threadIdx.x; i < nrows * (d / 4); i += nthreads) {
+        const int r = i / (d / 4), c4 = i % (d / 4);
+        reinterpret_cast<float4*>(qrows + r * d)[c4] =
+            __ldg(reinterpret_cast<const float4*>(qp + (long long)(row0 + r) * d) + c4);
+    }
+
+    // scores, tile by tile
+    for (int t0 = 0; t0 < C; t0 += kTile) {
+        __syncthreads();
+        const int tn = min(kTile, C - t0);
+        for (int i = threadIdx.x; i < tn * (d / 4); i += nthreads) {
+            const int r = i / (d / 4), c4 = i % (d / 4);
+            reinterpret_cast<float4*>(ktile + r * ktile_stride)[c4] =
+                __ldg(reinterpret_cast<const float4*>(kp + (long long)cand[t0 + r] * d) + c4);
+        }
+        __syncthreads();
+        if (warp < nrows) {
+            const float* qr = qrows + warp * d;
+            float acc0 = 0.f, acc1 = 0.f;
+            const float* k0 = ktile + lane * ktile_stride;
+            const float* k1 = ktile + (lane + 32) * ktile_stride;
+            for (int c = 0; c < d; c += 4) {
+                float4 q4 = *reinterpret_cast<const float4*>(qr + c);
+                float4 a4 = *reinterpret_cast<const float4*>(k0 + c);
+                float4 b4 = *reinterpret_cast<const float4*>(k1 + c);
+                acc0 = fmaf(q4.x, a4.x, acc0); acc0 = fmaf(q4.y, a4.y, acc0);
+                acc0 = fmaf(q4.z, a4.z, acc0); acc0 = fmaf(q4.w, a4.w, acc0);
+                acc1 = fmaf(q4.x, b4.x, acc1); acc1 = fmaf(q4.y, b4.y, acc1);
+                acc1 = fmaf(q4.z, b4.z, acc1); acc1 = fmaf(q4.w, b4.w, acc1);
+            }
+            if (lane < tn) scores[warp * C + t0 + lane] = acc0;
+            if (lane + 32 < tn) scores[warp * C + t0 + lane + 32] = acc1;
+        }
+    }
+    __syncthreads();
+    if (warp >= nrows) return;
+
+    // Top-K tournament for row `warp`
+    float s[CPL];
+    int idx[CPL];
+#pragma unroll
+    for (int m = 0; m < CPL; m++) {
+        const int c = lane + 32 * m;
+        if (c < C) {
+            float v = scores[warp * C + c];
+            s[m] = (v != v) ? -INFINITY : v;  // NaN never wins
+            idx[m] = cand[c];
+        } else {
+            s[m] = -INFINITY;
+            idx[m] = INT_MAX;
+        }
+    }
+    unsigned taken = 0;
+    int* krow = kept + warp * kMaxKeep;
+    for (int k = 0; k < a.Kl; k++) {
+        float bs = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int m = 0; m < CPL; m++)
+            if (!(taken >> m & 1u) && better(s[m], idx[m], bs, bi)) { bs = s[m]; bi = idx[m]; }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (better(os, oi, bs, bi)) { bs = os; bi = oi; }
+        }
+#pragma unroll
+        for (int m = 0; m < CPL; m++)
+            if (idx[m] == bi) taken |= 1u << m;
+        if (lane == 0) krow[k] = bi;
+    }
+    __syncwarp();
+    const int row = row0 + warp;
+    int* orow = a.out + slice * a.out_stride + (long long)row * a.Kl;
+    for (int k = lane; k < a.Kl; k += 32) {
+        const int v = krow[k];
+        int rank = 0;
+        for (int k2 = 0; k2 < a.Kl; k2++) rank += krow[k2] < v;
+        orow[rank] = v;
+    }
+    // enrichment index: every level-1 descendant of this row gets its rank-1
+    const int top1 = krow[0];
+    int* crow = a.coarse + (slice * a.T + (long long)row * a.span) * a.L + (a.level - 1);
+    for (int q = lane; q < a.span; q += 32) crow[(long long)q * a.L] = top1;
+}
+
+template <int CPL>
+int launch_level(const SelectArgs& a, long long slices, cudaStream_t st) {
+    const int grid_x = (a.n_l + a.rows_per_cta - 1) / a.rows_per_cta;
+    const size_t smem = sizeof(float) * (kTile * (a.d + 4) + kMaxRows * a.d + kMaxRows * a.C) +
+                        sizeof(int) * (a.C + kMaxRows * kMaxKeep);
+    if (smem > 200 * 1024 || slices > 65535) return LLSA_ERR_UNSUPPORTED;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(select_level_kernel<CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    LLSA_LAUNCH("select_level", st,
+                select_level_kernel<CPL><<<dim3(grid_x, (unsigned)slices), 32 * a.rows_per_cta, smem, st>>>(a));
+    return LLSA_OK;
+}
+
+}  // namespace
+
+int launch_select(const Shape& s, const float* pyr, int32_t* sel_idx, int32_t* coarse_idx, int32_t* level_idx,
+                  cudaStream_t st) {
+    const long long pyr_stride = (long long)s.P * s.d;
+    const float* qpyr = pyr;
+    const float* kpyr = pyr + s.slices * pyr_stride;
+    // rows per CTA: a divisor of B (siblings share a parent) of at most 16
+    int rpc = 1;
+    for (int r = 1; r <= kMaxRows; r++)
+        if (s.B % r == 0) rpc = r;
+    long long span = 1;
+    for (int l = 1; l < s.L; l++) span *= s.B;
+    for (int l = s.L; l >= 1; l--) {
+        SelectArgs a;
+        a.qpyr = qpyr;
+        a.kpyr = kpyr;
+        a.pyr_stride = pyr_stride;
+        a.row_off = s.row_offset[l];
+        a.n_l = s.n_level[l];
+        a.d = s.d;
+        a.B = s.B;
+        a.Kl = s.topk_level[l];
+        a.coarse = coarse_idx;
+        a.T = s.T;
+        a.L = s.L;
+        a.level = l;
+        a.span = (int)span;
+        a.status = status_ptr();
+        if (l == s.L) {
+            a.parent = nullptr;
+            a.parent_stride = 0;
+            a.Kp = 0;
+            a.C = s.n_level[l];
+            a.rows_per_cta = kMaxRows;
+            a.n_parent = 0;
+        } else {
+            a.parent = level_idx + s.level_idx_offset[l + 1];
+            a.parent_stride = s.level_idx_per_slice;
+            a.Kp = s.topk_level[l + 1];
+            a.C = a.Kp * s.B;
+            a.rows_per_cta = rpc;
+            a.n_parent = s.n_level[l + 1];
+        }
+        if (l == 1) {
+            a.out = sel_idx;
+            a.out_stride = (long long)s.T * s.K1;
+        } else {
+            a.out = level_idx + s.level_idx_offset[l];
+            a.out_stride = s.level_idx_per_slice;
+        }
+        if (a.C > kMaxCand || a.Kl > kMaxKeep) return LLSA_ERR_UNSUPPORTED;
+        const int cpl = (a.C + 31) / 32;
+        int rc;
+        if (cpl <= 1) rc = launch_level<1>(a, s.slices, st);
+        else if (cpl <= 2) rc = launch_level<2>(a, s.slices, st);
+        else if (cpl <= 4) rc = launch_level<4>(a, s.slices, st);
+        else if (cpl <= 8) rc = launch_level<8>(a, s.slices, st);
+        else if (cpl <= 16) rc = launch_level<16>(a, s.slices, st);
+        else rc = launch_level<32>(a, s.slices, st);
+        if (rc != LLSA_OK) return rc;
+        span /= s.B;
+    }
+    return LLSA_OK;
+}
+
+}  // namespace llsa
