@@ -1,0 +1,243 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, stage by
+stage and end to end, on seeded synthetic inputs that span several tiles and
+ragged tails, plus the method's degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import hierarchical_sparse_attention_mean_gb300 as llsa
+from hierarchical_sparse_attention_mean_gb300 import build, synth
+
+from parity import assert_close, assert_lse, check_selection, dev_inputs, gpu_stage_outputs, params_of
+
+pytestmark = pytest.mark.gpu
+
+W = synth.Workload
+CASES = {
+    # the 32x32 fp32 forward workload, full size
+    "n1024-fp32": synth.WORKLOADS["llsa-fwd-n1024-d64-b1h1-K4-fp32"],
+    # the 64x64 bf16 forward workload, full size (16 slices)
+    "n4096-bf16": synth.WORKLOADS["llsa-fwd-n4096-d64-b2h8-K8-bf16"],
+    # 768 query blocks: not a multiple of the SM count
+    "ragged-h3": W("ragged", 1, 3, 4096, 64, amplitude=0.5, seed=77),
+    "d128-K16": W("d128", 1, 2, 4096, 128, topk=16, amplitude=0.5, seed=78),
+    "B4-L4-fp32": W("b4", 1, 2, 1024, 32, block=4, topk=3, dtype="fp32", seed=79),
+    "B2-fig1": W("fig1", 1, 1, 8, 8, block=2, topk=1, dtype="fp32", seed=80),
+    "B8-d16-bf16": W("b8", 2, 1, 512, 16, block=8, topk=5, amplitude=0.5, seed=81),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    oracle.build()
+
+
+def run_oracle(w, x, **kw):
+    return oracle.run(x["q"], x["k"], x["v"], x.get("dout"), B=w.block, K=w.topk, threads=16, **kw)
+
+
+@pytest.fixture(scope="module")
+def case_data():
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            w = CASES[name]
+            x = synth.make_inputs(w)
+            cache[name] = (w, x, run_oracle(w, x))
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_pool(case_data, name):
+    w, x, ref = case_data(name)
+    out, _ = gpu_stage_outputs(w, x, backward=False)
+    for s, r in enumerate(ref["slices"]):
+        for t, key in enumerate(("qpyr", "kpyr", "vpyr")):
+            err = np.abs(out["pyr"][t, s] - r[key]).max()
+            assert err <= 1e-5 * max(1.0, np.abs(r[key]).max()), (s, key, err)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_select(case_data, name):
+    w, x, ref = case_data(name)
+    out, _ = gpu_stage_outputs(w, x, backward=False)
+    L = ref["L"]
+    total = 0
+    for s, r in enumerate(ref["slices"]):
+        levels = [None] + [out["gpu_levels"][l][s] for l in range(1, L + 1)]
+        differ, T = check_selection(r["qpyr"], r["kpyr"], w.n, w.block, L, w.topk, levels,
+                                    out["gpu_coarse"][s], r["sel"])
+        total += len(differ)
+    assert total <= max(1, 0.01 * w.bh * (w.n // w.block)), total
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fwd_with_oracle_indices(case_data, name):
+    w, x, ref = case_data(name)
+    out, _ = gpu_stage_outputs(w, x, backward=False, oracle_sel=ref["slices"])
+    assert_close("o", out["o"], ref["o"], w.dtype)
+    assert_lse(out["lse"], ref["lse"])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_transpose_bit_exact(case_data, name):
+    w, x, ref = case_data(name)
+    out, _ = gpu_stage_outputs(w, x, backward=False, oracle_sel=ref["slices"])
+    for s, r in enumerate(ref["slices"]):
+        np.testing.assert_array_equal(out["col_ptr"][s], r["col_ptr"])
+        np.testing.assert_array_equal(out["row_idx"][s], r["row_idx"])
+
+
+@pytest.mark.parametrize("name", [n for n in CASES if CASES[n].backward])
+def test_bwd_with_oracle_indices(case_data, name):
+    w, x, ref = case_data(name)
+    out, _ = gpu_stage_outputs(w, x, backward=True, oracle_sel=ref["slices"])
+    for key in ("dq", "dk", "dv"):
+        assert_close(key, out[key], ref[key], w.dtype)
+
+
+def compare_end_to_end(w, ref, out):
+    """Outputs compared wherever the GPU and oracle selections agree; where
+    they differ the swaps were shown legal by check_selection."""
+    L, B = ref["L"], w.block
+    excluded = 0
+    for s, r in enumerate(ref["slices"]):
+        levels = [None] + [out["gpu_levels"][l][s] for l in range(1, L + 1)]
+        differ, T = check_selection(r["qpyr"], r["kpyr"], w.n, B, L, w.topk, levels, out["gpu_coarse"][s],
+                                    r["sel"])
+        tok = np.ones(w.n, bool)
+        kblk = np.ones(T, bool)
+        for i in differ:
+            tok[i * B:(i + 1) * B] = False
+            for row in (out["gpu_sel"][s][i], r["sel"]["levels"][1][i]):
+                kblk[row] = False
+            for crow in (out["gpu_coarse"][s][i], r["sel"]["coarse"][i]):
+                for l in range(1, L + 1):
+                    span = B ** (l - 1)
+                    kblk[crow[l - 1] * span:(crow[l - 1] + 1) * span] = False
+        excluded += len(differ)
+        ktok = np.repeat(kblk, B)
+        assert_close("o", out["o"][s][tok], r["o"][tok], w.dtype)
+        assert_lse(out["lse"][s][tok], r["lse"][tok])
+        if "dq" in out:
+            assert_close("dq", out["dq"][s][tok], r["dq"][tok], w.dtype)
+            assert_close("dk", out["dk"][s][ktok], r["dk"][ktok], w.dtype)
+            assert_close("dv", out["dv"][s][ktok], r["dv"][ktok], w.dtype)
+    return excluded
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_end_to_end(case_data, name):
+    w, x, ref = case_data(name)
+    out, _ = gpu_stage_outputs(w, x, backward=w.backward)
+    excluded = compare_end_to_end(w, ref, out)
+    assert excluded <= max(1, 0.01 * w.bh * (w.n // w.block))
+
+
+# ------------------------------------------------------------ edge cases
+
+def test_constant_inputs_tie_break_bit_exact():
+    """Every score ties: the lower index wins at every level, on both sides."""
+    w = W("const", 1, 2, 4096, 64, seed=1)
+    x = {k: np.full((2, 4096, 64), 0.5, np.float32) for k in ("q", "k", "v", "dout")}
+    ref = run_oracle(w, x)
+    out, _ = gpu_stage_outputs(w, x)
+    for s, r in enumerate(ref["slices"]):
+        np.testing.assert_array_equal(out["gpu_sel"][s], r["sel"]["levels"][1])
+        np.testing.assert_array_equal(out["gpu_coarse"][s], r["sel"]["coarse"])
+        np.testing.assert_array_equal(out["gpu_levels"][2][s], r["sel"]["levels"][2])
+    assert_close("o", out["o"], ref["o"], "bf16")
+    for key in ("dq", "dk", "dv"):
+        assert_close(key, out[key], ref[key], "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp32"])
+def test_full_selection_is_dense_plus_enrichment(dtype):
+    """K*B >= N: every block selected; equals dense attention over all tokens
+    plus the enrichment tokens."""
+    w = W("full", 1, 2, 1024, 32, topk=64, dtype=dtype, amplitude=0.5, seed=5)
+    x = synth.make_inputs(w)
+    ref = run_oracle(w, x)
+    out, _ = gpu_stage_outputs(w, x)
+    assert (out["gpu_sel"] == np.arange(64)[None, None, :]).all()
+    assert_close("o", out["o"], ref["o"], dtype)
+    assert_lse(out["lse"], ref["lse"])
+    for key in ("dq", "dk", "dv"):
+        assert_close(key, out[key], ref[key], dtype)
+
+
+def test_no_enrichment_is_sparse_softmax():
+    w = W("noenr", 1, 2, 4096, 64, amplitude=0.5, seed=6)
+    x = synth.make_inputs(w)
+    ref = run_oracle(w, x, Le=0)
+    out, _ = gpu_stage_outputs(w, x, p=params_of(w, enrich_levels=0), oracle_sel=ref["slices"])
+    assert_close("o", out["o"], ref["o"], "bf16")
+    assert_lse(out["lse"], ref["lse"])
+    for key in ("dq", "dk", "dv"):
+        assert_close(key, out[key], ref[key], "bf16")
+
+
+def test_partial_enrichment_and_fewer_levels():
+    w = W("le1", 1, 2, 16384, 64, amplitude=0.5, seed=7)
+    x = synth.make_inputs(w)
+    ref = run_oracle(w, x, L=1, Le=1)
+    out, _ = gpu_stage_outputs(w, x, p=params_of(w, levels=1, enrich_levels=1), oracle_sel=ref["slices"])
+    assert_close("o", out["o"], ref["o"], "bf16")
+    for key in ("dq", "dk", "dv"):
+        assert_close(key, out[key], ref[key], "bf16")
+
+
+def test_empty_batch_is_a_no_op():
+    p = llsa.Params(0, 4, 4096, 64)
+    z = torch.empty((0, 4, 4096, 64), dtype=torch.bfloat16, device="cuda")
+    b = llsa.Buffers(p)
+    llsa.forward(p, z, z, z, b)
+    llsa.backward(p, z, z, z, z, b)
+    torch.cuda.synchronize()
+
+
+def test_out_of_range_index_sets_status():
+    """An index outside [0, T) is caught by the kernel's bounds check: the
+    access is clamped and the device status word reports it."""
+    w = W("bad", 1, 1, 4096, 64, amplitude=0.5, seed=8)
+    x = dev_inputs(w, synth.make_inputs(w, with_dout=False))
+    p = params_of(w)
+    b = llsa.forward(p, x["q"], x["k"], x["v"])
+    torch.cuda.synchronize()
+    assert llsa.llsa_get_status() == 0
+    b.sel_idx[0, 3, 2] = 10_000
+    llsa.llsa_fwd(p, x["q"], x["k"], x["v"], b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse)
+    assert llsa.llsa_get_status() == -10
+    assert llsa.llsa_get_status() == 0   # reading clears it
+
+
+def test_autograd_function_matches_direct_calls():
+    w = W("ag", 1, 2, 4096, 64, amplitude=0.5, seed=9)
+    x = dev_inputs(w, synth.make_inputs(w))
+    q, k, v = (x[a].clone().requires_grad_(True) for a in ("q", "k", "v"))
+    o = llsa.llsa_attention(q, k, v, block=16, topk=8)
+    o.backward(x["dout"])
+    p = params_of(w)
+    b = llsa.forward(p, x["q"], x["k"], x["v"])
+    dq, dk, dv = llsa.backward(p, x["q"], x["k"], x["v"], x["dout"], b)
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), b.o)
+    assert torch.equal(q.grad, dq) and torch.equal(k.grad, dk) and torch.equal(v.grad, dv)
+
+
+def test_deterministic_across_runs():
+    w = W("det", 1, 3, 4096, 64, amplitude=0.5, seed=10)
+    x = dev_inputs(w, synth.make_inputs(w))
+    p = params_of(w)
+    outs = []
+    for _ in range(2):
+        b = llsa.forward(p, x["q"], x["k"], x["v"])
+        g = llsa.backward(p, x["q"], x["k"], x["v"], x["dout"], b)
+        outs.append([b.o.clone(), b.lse.clone(), b.col_ptr.clone(), b.row_idx.clone()] + [t.clone() for t in g])
+    torch.cuda.synchronize()
+    for a, c in zip(*outs):
+        assert torch.equal(a, c)
