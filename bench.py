@@ -1,0 +1,400 @@
+"""Benchmark of the LLSA hot path on GB300: one step = pool -> select ->
+forward -> index transpose -> backward over one batch of synthetic inputs
+already resident in HBM (256x256 pixel tokens by default), timed with CUDA
+events. Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl llsa|reference]
+
+Under torchrun (N > 1) every rank runs its own independent problem of the
+same size (weak scaling, no collective on the data path); the rank times are
+reduced with MAX. `--impl reference` times the CPU oracle on a bounded sample
+of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from hierarchical_sparse_attention_mean_gb300 import synth  # noqa: E402
+
+METRIC = "LLSA fwd+bwd ms & effective TFLOP/s at N=65536 (1×GB300); % of roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+SMS, FP32_LANES_PER_SM = 152, 128
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p.get(k, FALLBACK_PEAKS[k])) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------- work model
+
+def work_model(w: synth.Workload, s) -> dict:
+    """Algorithmic work of one step (useful sparse work only)."""
+    bh, n, d = w.bh, w.n, w.d
+    es = 2 if w.dtype == "bf16" else 4
+    pairs = bh * n * s.keys_per_query                 # (query, key) pairs incl. coarse tokens
+    fine_pairs = bh * n * s.topk_level[1] * w.block
+    tok = bh * n * d * es                             # bytes of one token tensor
+    P = s.pyr_rows
+    scored = s.n_level[s.levels] ** 2 + sum(s.n_level[l] * s.topk_level[l + 1] * w.block
+                                             for l in range(1, s.levels))
+    return {
+        "pairs": pairs,
+        "fwd_flops": 4 * d * pairs,
+        "bwd_flops": 10 * d * pairs,
+        "step_flops": 14 * d * pairs,
+        "select_flops": 2 * d * scored * bh,
+        # per kernel: (bytes, flops) that the kernel's algorithm needs
+        "kernels": {
+            "pool_chunk": (3 * tok + 3 * bh * P * d * 4, 0),
+            "fwd": (4 * tok + bh * n * 4, 4 * d * pairs),
+            "bwd_dq": (4 * tok + bh * n * 8, 6 * d * pairs),
+            "bwd_dkv": (6 * tok + bh * n * 8, 8 * d * fine_pairs),
+            "transpose": (4 * bh * s.n_blocks * s.topk_level[1] * 3, 0),
+            "select_level": (0, 2 * d * scored * bh),
+        },
+    }
+
+
+def kernel_key(name: str) -> str:
+    for key in ("pool_chunk", "bwd_dq", "bwd_dkv", "select_level", "coarse_reduce"):
+        if name.startswith(key):
+            return key
+    if name.startswith("fwd"):
+        return "fwd"
+    if name.startswith("transpose"):
+        return "transpose"
+    return name
+
+
+def kernel_bound(key, avg_ms, work, peaks, tensor_path):
+    """Roofline of one kernel: the resource whose ideal time is longest."""
+    nbytes, flops = work["kernels"].get(key, (0, 0))
+    t = avg_ms * 1e-3
+    hbm_t = nbytes / (peaks["hbm_gbs"] * 1e9) if nbytes else 0.0
+    if tensor_path:
+        cpeak, cunit, cbound = peaks["bf16_tflops_sustained"], "TFLOP/s", "tensor"
+    else:
+        cpeak = SMS * FP32_LANES_PER_SM * 2 * peaks["sm_max_mhz"] * 1e6 / 1e12
+        cunit, cbound = "TFLOP/s", "alu"
+    c_t = flops / (cpeak * 1e12) if flops else 0.0
+    if hbm_t >= c_t:
+        ach = nbytes / t / 1e9
+        return {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm_gbs"], 4), "algorithmic_bytes": nbytes}
+    ach = flops / t / 1e12
+    return {"bound": cbound, "achieved": round(ach, 2), "peak": round(cpeak, 1), "unit": cunit,
+            "frac": round(ach / cpeak, 4), "algorithmic_flops": flops}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_llsa(args, ws, rank, local):
+    import hierarchical_sparse_attention_mean_gb300 as llsa
+    from hierarchical_sparse_attention_mean_gb300 import build
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    w0 = synth.WORKLOADS[args.workload]
+    # each rank: an independent problem of the same size (weak scaling)
+    w = synth.Workload(**{**w0.__dict__, "seed": w0.seed + 7919 * rank})
+    x = synth.make_inputs(w, threads=os.cpu_count() or 8)
+    shape = (w.batch, w.heads, w.n, w.d)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    host = {k: torch.from_numpy(v).to(td).reshape(shape).pin_memory() for k, v in x.items()}
+    d = {k: v.to(dev) for k, v in host.items()}
+    p = llsa.Params(w.batch, w.heads, w.n, w.d, block=w.block, topk=w.topk, dtype=w.dtype)
+    s = llsa.get_sizes(p)
+    b = llsa.Buffers(p, dev)
+    dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        llsa.forward(p, d["q"], d["k"], d["v"], b)
+        llsa.backward(p, d["q"], d["k"], d["v"], d["dout"], b, dq, dk, dv)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if llsa.llsa_get_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    # ---- timed region: K device-resident steps
+    sampler = ClockSampler(torch.cuda.current_device())
+    llsa.profile_reset()
+    llsa.profile_enable(True)
+    sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    launches0 = llsa.llsa_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    launches = llsa.llsa_launch_count() - launches0
+    llsa.profile_enable(False)
+    records = llsa.profile_read(cap=64 * args.steps + 64)
+    elapsed = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([elapsed], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed = float(t.item())
+    ms_step = elapsed / args.steps
+
+    # per-kernel durations from the events recorded around each launch
+    per = {}
+    for name, ms in records:
+        k = kernel_key(name)
+        tot, cnt = per.get(k, (0.0, 0))
+        per[k] = (tot + ms, cnt + 1)
+    stage_ms = {k: round(t / args.steps, 4) for k, (t, c) in per.items()}
+    peaks, peak_src = load_peaks()
+    work = work_model(w, s)
+    dom = max(per, key=lambda k: per[k][0])
+    avg_ms = per[dom][0] / per[dom][1]
+    tensor_path = dom in llsa_tensor_kernels(records)
+    roof = kernel_bound(dom, avg_ms, work, peaks, tensor_path)
+    roof.update({"kernel": dom, "avg_launch_ms": round(avg_ms, 4), "peak_source": peak_src,
+                 "traffic": args.traffic})
+
+    # ---- end to end through host buffers: H2D inputs, step, D2H outputs
+    e2e_steps = max(3, min(args.steps, 20))
+    hout = {k: torch.empty(shape, dtype=td).pin_memory() for k in ("o", "dq", "dk", "dv")}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    barrier()
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(e2e_steps):
+        for k in d:
+            d[k].copy_(host[k], non_blocking=True)
+        step()
+        hout["o"].copy_(b.o, non_blocking=True)
+        hout["dq"].copy_(dq, non_blocking=True)
+        hout["dk"].copy_(dk, non_blocking=True)
+        hout["dv"].copy_(dv, non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e2.elapsed_time(e3) / e2e_steps
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    status = llsa.llsa_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    value = ws * work["step_flops"] / (ms_step * 1e-3) / 1e12
+    out = {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w0.name, "batch": w.batch, "heads": w.heads, "n": w.n, "d": w.d, "block": w.block,
+                   "topk": w.topk, "levels": s.levels, "enrich_levels": s.enrich_levels,
+                   "keys_per_query": s.keys_per_query, "inputs": f"{w.kind}, seed {w0.seed} (+7919 per rank)",
+                   "l2": "no flush: the step's inputs (4 x %.0f MB) exceed the 129 MB L2" % (h2d / 4 / 1e6),
+                   "parallelism": f"replicas{ws}", "step": "pool+select+fwd+transpose+bwd",
+                   "flops_per_step": work["step_flops"], "flops_counted": "14*d per (query, key) pair: "
+                   "fwd 4d, bwd 10d (S, dP, dV, dK, dQ); selection excluded"},
+        "stage_ms": stage_ms,
+        "roofline": roof,
+        "e2e": {"value": round(ws * work["step_flops"] / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, x, s)
+    return out
+
+
+def llsa_tensor_kernels(records):
+    return {kernel_key(n) for n, _ in records if n.endswith("_tc")}
+
+
+def cpu_baseline(w, x, s):
+    """The oracle as it stands, the whole path on one slice per host thread."""
+    import oracle
+    oracle.build()
+    n_sl = max(1, min(os.cpu_count() or 1, w.bh))
+    t0 = time.perf_counter()
+    oracle.run(x["q"][:n_sl], x["k"][:n_sl], x["v"][:n_sl], x["dout"][:n_sl], B=w.block, K=w.topk, threads=n_sl)
+    wall = time.perf_counter() - t0
+    flops = 14 * w.d * n_sl * w.n * s.keys_per_query
+    return {"value": round(flops / wall / 1e12, 6), "unit": "TFLOP/s", "cores": n_sl, "kind": "oracle",
+            "wall_s": round(wall, 2),
+            "sample": f"whole path (pool, select, fwd, transpose, bwd) of {n_sl} of {w.bh} (batch, head) slices, "
+                      "one oracle thread per slice, fp64"}
+
+
+# --------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle timed as it stands, on a bounded sample of the same
+    workload: pooling, selection and the forward of slice 0 are prepared once;
+    each step then runs the oracle forward and backward (dq of R query tokens,
+    dk/dv of R/B key blocks), R sized so the whole run stays within minutes."""
+    import oracle
+    oracle.build()
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_slice(w, 0)
+    B, K, d, n = w.block, w.topk, w.d, w.n
+    L = oracle.num_levels(n, B)
+    scale = 1.0 / math.sqrt(d)
+    qp, kp, vp = (oracle.pool(x[t], B, L) for t in ("q", "k", "v"))
+    sel = oracle.select_all(qp, kp, n, B, L, K)
+    I1, coarse = sel["levels"][1], sel["coarse"]
+    o, lse = oracle.fwd(x["q"], x["k"], x["v"], kp, vp, B, L, L, I1, coarse, scale)
+    kpq = I1.shape[1] * B + L
+
+    def one(start, R):
+        rows = (np.arange(R) + start) % n
+        blocks = (np.arange(R // B) + start // B) % (n // B)
+        oracle.fwd(x["q"], x["k"], x["v"], kp, vp, B, L, L, I1, coarse, scale, qlist=rows)
+        oracle.bwd_dq_rows(x["q"], x["k"], x["v"], kp, vp, o[rows], lse[rows], x["dout"], B, L, L, I1, coarse,
+                           scale, rows)
+        oracle.bwd_dkv_blocks(x["q"], x["k"], x["v"], kp, vp, o, lse, x["dout"], B, L, L, I1, coarse, scale,
+                              blocks)
+
+    budget_s = min(1.0, 100.0 / max(1, args.steps + args.warmup))
+    R = 256
+    t0 = time.perf_counter()
+    one(0, R)
+    dt = time.perf_counter() - t0
+    R = int(max(B, min(n, R * budget_s / max(dt, 1e-6))) // B * B)
+    for i in range(args.warmup):
+        one(i * R, R)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one((args.warmup + i) * R, R)
+    wall = time.perf_counter() - t0
+    ms = wall / args.steps * 1e3
+    value = 14 * d * R * kpq / (ms * 1e-3) / 1e12
+    sample = (f"per step: oracle fwd + dq of {R} query tokens and dk/dv of {R // B} key blocks of slice 0 "
+              f"(pool/select/fwd of that slice prepared before timing); 14*d FLOPs per (query, key) pair")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "n": n, "d": d, "block": B,
+                       "topk": K, "levels": L},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["llsa", "reference"], default="llsa")
+    ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture of this build")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl")
+    try:
+        out = run_llsa(args, ws, rank, local)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+    finally:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
