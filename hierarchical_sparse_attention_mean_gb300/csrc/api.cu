@@ -77,6 +77,8 @@ cudaEvent_t take_event() {
 }
 }  // namespace
 
+int device_ready() { return check_device(); }
+
 int* status_ptr() {
     int dev = current_device();
     return dev < 0 ? nullptr : g_status_addr[dev];

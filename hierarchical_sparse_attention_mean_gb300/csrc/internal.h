@@ -67,6 +67,10 @@ int* status_ptr();
 // Number of SMs of the current device.
 int sm_count();
 
+// LLSA_OK when the current device is a GB300 (compute capability 10.3); also
+// sets up the per-device status word on first use.
+int device_ready();
+
 // ---------------------------------------------------------------- launchers
 
 int launch_pool(const Shape& s, const void* q, const void* k, const void* v, float* pyr, cudaStream_t st);

@@ -165,6 +165,29 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
              const int32_t *coarse_idx, const int32_t *col_ptr, const int32_t *row_idx,
              void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, void *stream);
 
+/* Sparse index transpose for callers that cannot allocate device memory.
+ * No counterpart in the paper: this is a deployment variant of
+ * llsa_index_transpose for callers that may not call cudaMalloc or hand over a
+ * workspace (an allocator-free runtime, a caller inside someone else's memory
+ * pool or budget). Same inputs, outputs, layout and results as
+ * llsa_index_transpose, without `ws`: its scratch -- one int32 counter per
+ * fine key block per slice -- lives in a fixed device array of
+ * LLSA_NOALLOC_TRANSPOSE_MAX_COUNTERS entries (4 MiB) that every GPU which
+ * loads this library holds until the process exits.
+ *   - Limit: batch * heads * T <= LLSA_NOALLOC_TRANSPOSE_MAX_COUNTERS, else
+ *     LLSA_ERR_UNSUPPORTED and nothing is enqueued.
+ *   - Allocation: none; no cudaMalloc, cudaFree or allocating library call.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Sharing: every call uses the same array. It is zeroed on the stream at
+ *     the start of each call, so no earlier contents leak into a result, but
+ *     calls whose kernels overlap on the GPU (different streams, no ordering)
+ *     race on it and give wrong results. */
+#define LLSA_NOALLOC_TRANSPOSE_MAX_COUNTERS (1 << 20)
+int llsa_index_transpose_noalloc(const llsa_params *p, const int32_t *sel_idx, int32_t *col_ptr, int32_t *row_idx,
+                                 void *stream);
+
 /* Reads (after synchronising `stream`) and clears the device status word of
  * the current device: LLSA_OK, LLSA_ERR_TIMEOUT or LLSA_ERR_BAD_INDEX. */
 int llsa_get_status(void *stream, int *device_status);
