@@ -11,6 +11,7 @@ int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, cons
     a.kpyr = pyr + s.slices * a.pyr_stride;
     a.vpyr = pyr + 2 * s.slices * a.pyr_stride;
     a.sel = sel_idx; a.coarse = coarse_idx; a.out_o = o; a.lse = lse;
+    if (fwd_tc_supported(s)) return launch_fwd_tc(s, a, st);
     return launch_fwd_simt(s, a, st);
 }
 

@@ -32,6 +32,10 @@ int launch_bwd_dq_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 
+// tensor-core kernels (bf16, B = 16, d in {64, 128}, K_1 in {8, 16})
+bool fwd_tc_supported(const Shape& s);
+int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
+
 // Adds to the fine-key gradients of column chunk c4 of key block j the
 // gradients of the pooled tokens above it: the level-l ancestor of block j is
 // j / B^(l-1); each of its B^l fine rows receives 1/B^l of its gradient.

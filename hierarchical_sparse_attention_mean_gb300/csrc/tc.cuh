@@ -1,0 +1,215 @@
+// tc.cuh -- sm_103a building blocks for the tensor-core kernels: tcgen05 MMA
+// with operands in shared memory and accumulators in tensor memory (TMEM), TMA
+// tile loads, mbarriers with bounded waits.
+//
+// Encodings (checked on a GB300 before use):
+//   shared-memory matrix descriptor: start >> 4 in bits 0-13, leading byte
+//   offset >> 4 in 16-29, stride byte offset >> 4 in 32-45, version 1 at bit 46,
+//   layout 2 (128-byte swizzle) in bits 61-63. With 128-byte rows the swizzle
+//   atom is 8 rows = 1024 B: K-major operands use SBO = 1024 and step along K by
+//   moving the start address 32 B per 16 bf16; MN-major operands store rows of
+//   64 MN-elements per K index, SBO = 1024 (8 K rows), LBO = the distance
+//   between 64-wide MN regions, and step along K by 16 rows (2048 B).
+//   instruction descriptor (kind::f16): D f32 (bit 4), A, B bf16 (bits 7, 10),
+//   A / B MN-major flags (bits 15, 16), N >> 3 (bits 17-22), M >> 4 (24-28).
+//   TMEM accumulator of an M = 128 MMA: row r in lane r; of an M = 64 MMA: row
+//   r in lane 32 * (r / 16) + r % 16 (the first 16 lanes of each quarter).
+#pragma once
+
+#include <cuda.h>
+
+#include "internal.h"
+
+namespace llsa {
+namespace tc {
+
+constexpr int kSpinLimit = 1 << 22;  // bounded waits: ~ seconds, then LLSA_ERR_TIMEOUT
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+    d |= 1ull << 46;
+    d |= 2ull << 61;
+    return d;
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D (TMEM) (+)= A (smem) * B (smem); one thread issues.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                 :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// Arrives on the mbarrier once every MMA issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit(uint32_t mbar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n"
+                 :: "r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t mbar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" :: "r"(mbar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" :: "r"(mbar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" :: "r"(mbar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok) : "r"(mbar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Waits for the phase of the given parity to complete. Gives up after a
+// bounded number of polls, or as soon as another thread of the CTA gave up
+// (abort flag), recording LLSA_ERR_TIMEOUT; returns false then.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status) {
+    for (int it = 0; it < kSpinLimit; it++) {
+        if (mbar_try(mbar, parity)) return true;
+        if ((it & 63) == 63 && *abort_flag) return false;
+    }
+    *abort_flag = 1;
+    set_status(status, LLSA_ERR_TIMEOUT);
+    return false;
+}
+
+// 2D tiled TMA load (box from the tensor map) into shared memory, completing
+// bytes on the mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t mbar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar) : "memory");
+}
+
+// 1D bulk copy global -> shared (16-byte aligned addresses, size a multiple
+// of 16), completing bytes on the mbarrier.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(mbar) : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared through L2 (not L1).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" :: "r"(dst), "l"(src) : "memory");
+}
+
+// Arrives on the mbarrier once every cp.async issued so far by this thread
+// has landed (the arrival is counted in the barrier's initial count).
+__device__ __forceinline__ void cp_async_arrive(uint32_t mbar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" :: "r"(mbar) : "memory");
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 1/x with the hardware approximation (relative error about 2^-23).
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// Whole warp: allocate ncols TMEM columns, address written to smem slot.
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" :: "r"(slot), "r"(ncols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" :: "r"(taddr), "r"(ncols));
+}
+
+// 32 lanes x 16 consecutive 32-bit columns; lane i of the warp reads TMEM
+// lane (taddr.lane + i). Includes the wait for completion.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;\n" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// Byte offset of element (row, col) of a tile stored as 128-byte swizzled
+// rows of 64 bf16, with regions of `region_rows` rows per 64 columns.
+__device__ __forceinline__ uint32_t sw128_offset(int row, int col, int region_rows) {
+    const int region = col >> 6, c = col & 63;
+    return (uint32_t)(region * region_rows * 128 + row * 128 + ((((c >> 3) ^ (row & 7))) << 4) + ((c & 7) << 1));
+}
+
+// Reduces 16 values per lane across the warp so that lanes 2c and 2c+1 end up
+// holding the reduction of column c (16 shuffles instead of 80).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(const float* v, int lane) {
+    auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+    float w8[8], w4[4], w2[2];
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        const float send = b4 ? v[i] : v[i + 8];
+        const float keep = b4 ? v[i + 8] : v[i];
+        w8[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float send = b3 ? w8[i] : w8[i + 4];
+        const float keep = b3 ? w8[i + 4] : w8[i];
+        w4[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    }
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        const float send = b2 ? w4[i] : w4[i + 2];
+        const float keep = b2 ? w4[i + 2] : w4[i];
+        w2[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    }
+    const float send = b1 ? w2[0] : w2[1];
+    const float keep = b1 ? w2[1] : w2[0];
+    float r = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    return op(r, __shfl_xor_sync(0xffffffffu, r, 1));
+}
+
+}  // namespace tc
+
+// Host: a 2D bf16 tensor map over a row-major [rows, cols] matrix with a box
+// of 16 rows x 64 columns and 128-byte swizzle (the layout the descriptors
+// above describe). Returns LLSA_OK or LLSA_ERR_CUDA.
+int make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, int cols, int box_rows);
+
+}  // namespace llsa
