@@ -26,6 +26,11 @@ int launch_bwd(const Shape& s, const void* q, const void* k, const void* v, cons
     a.sel = sel_idx; a.coarse = coarse_idx; a.col_ptr = col_ptr; a.row_idx = row_idx;
     a.dq = dq; a.dk = dk; a.dv = dv;
     carve_bwd_workspace(s, ws, &a);
+    if (fwd_tc_supported(s) && bwd_dkv_tc_fits(s)) {
+        LLSA_TRY(launch_bwd_dq_tc(s, a, st));
+        LLSA_TRY(launch_coarse_reduce(s, a, st));
+        return launch_bwd_dkv_tc(s, a, st);
+    }
     LLSA_TRY(launch_bwd_dq_simt(s, a, st));
     LLSA_TRY(launch_coarse_reduce(s, a, st));
     return launch_bwd_dkv_simt(s, a, st);

@@ -35,6 +35,9 @@ int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 // tensor-core kernels (bf16, B = 16, d in {64, 128}, K_1 in {8, 16})
 bool fwd_tc_supported(const Shape& s);
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
+int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
+bool bwd_dkv_tc_fits(const Shape& s);
+int launch_bwd_dkv_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
 
 // Adds to the fine-key gradients of column chunk c4 of key block j the
 // gradients of the pooled tokens above it: the level-l ancestor of block j is

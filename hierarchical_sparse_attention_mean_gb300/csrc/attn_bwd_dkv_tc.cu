@@ -1,0 +1,423 @@
+// attn_bwd_dkv_tc.cu -- backward, key-major part, on the tcgen05 tensor cores
+// (bf16, B = 16, d in {64, 128}): dk, dv of every fine key block from the
+// query blocks that selected it, plus the pooled-level gradients.
+//
+// Method: Pith review of arXiv 2512.16615, "What carries the argument" (the
+// sparse-index transpose gives each key block its query blocks without a
+// dense N x N mask) and the referee's Sec. 4.3 / Figure 4 comments (sparse
+// key-value backward). For fine key block j and every query block i in CSC
+// column j: dv_j += P^T dO_i, dk_j += scale dS^T q_i, with P and dS recomputed
+// from q, k, v, dO, lse and D. Then dk_t += sum_l dK^(l)[anc] / B^l (and dv
+// likewise) for the pooled tokens above j.
+//
+// The column's query blocks are stacked eight at a time (M = 128 query rows):
+// S = Q_stack K_j^T and dP = dO_stack V_j^T (N = 16 keys), one TMEM lane per
+// query row, so P and dS need only that row's lse and D; then
+// dv^T += dO_stack^T P and dk^T += Q_stack^T dS (M = d, N = 16, K = 128 rows)
+// accumulate in TMEM across the column's groups, in CSC order (deterministic).
+// Each (key block, group of eight) is one item; items follow the key blocks of
+// the CTA in order; the two warpgroups take alternate key blocks.
+#include <algorithm>
+
+#include "attn.h"
+#include "tc.cuh"
+
+namespace llsa {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 384;
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxKeyBlocks = 2048;  // key blocks per CTA (counts kept in shared memory)
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct Cfg {
+    static constexpr int REG = D / 64;
+    static constexpr int QS_BYTES = 128 * D * 2;  // eight stacked 16-row query blocks
+    static constexpr int KB_BYTES = 16 * D * 2;
+    // Q stack, dO stack, K_j, V_j, (lse, D) pairs of the 128 rows
+    static constexpr int OFF_DO = QS_BYTES, OFF_K = 2 * QS_BYTES, OFF_V = OFF_K + KB_BYTES;
+    static constexpr int OFF_LD = OFF_V + KB_BYTES;
+    static constexpr int STAGE_BYTES = OFF_LD + 1024;
+    static constexpr int PB_BYTES = 16 * 128 * 2;  // P^T or dS^T of one item
+    static constexpr int FIXED = 4 * PB_BYTES + 4096 + kMaxKeyBlocks * 8;
+    static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
+    static constexpr int NPROD = STAGES_RAW >= 3 ? 3 : (STAGES_RAW >= 2 ? 2 : 1);
+    static constexpr int SPP = (STAGES_RAW < 1 ? 1 : (STAGES_RAW > 6 ? 6 : STAGES_RAW)) / NPROD;
+    static constexpr int STAGES = NPROD * SPP;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
+};
+
+template <class C>
+__device__ __forceinline__ void stage_of(int n, int& st, int& u) {
+    const int k = n / C::NPROD;
+    st = (n % C::NPROD) * C::SPP + k % C::SPP;
+    u = k / C::SPP;
+}
+
+struct Misc {
+    // per warpgroup, each used in that group's own item order
+    uint64_t full[6], empty[6], q_ready[2], s_full[2], s_free[2], p_full[2], p_free[2], acc_full[2], acc_free[2], drain;
+    uint32_t tmem_slot;
+    int abort_flag;
+    int n_kb, n_items;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
+                  const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, AttnArgs a) {
+    using C = Cfg<D>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* stages = sm;
+    unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;  // [warpgroup][P^T, dS^T]
+    Misc* ms = reinterpret_cast<Misc*>(pbuf + 4 * C::PB_BYTES);
+    int* kcnt = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(ms) + 4096);  // per key block: column count
+    int* kitem = kcnt + kMaxKeyBlocks;                                                  // first item of the key block
+    volatile int* abort_flag = &ms->abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long total = a.slices * (long long)a.T;
+    const int G = gridDim.x;
+    const int n_kb = total > blockIdx.x ? (int)((total - blockIdx.x + G - 1) / G) : 0;
+
+    // stages start zeroed: rows of an item's unused query blocks keep finite
+    // values (zeros or an earlier block), so P = dS = 0 there stays exact
+    for (int x = threadIdx.x; x < C::STAGES * C::STAGE_BYTES / 16; x += kThreads)
+        reinterpret_cast<uint4*>(stages)[x] = make_uint4(0, 0, 0, 0);
+    // column counts of this CTA's key blocks and the running item count
+    for (int kb = threadIdx.x; kb < n_kb; kb += kThreads) {
+        const long long g = blockIdx.x + (long long)kb * G;
+        const long long slice = g / a.T;
+        const int j = (int)(g - slice * a.T);
+        const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
+        const int b = cp[j], e = cp[j + 1];
+        // a column outside [0, T*K_1] is reported and treated as empty
+        const bool good = b >= 0 && e >= b && e <= a.K1 * a.T;
+        if (!good) set_status(a.status, LLSA_ERR_BAD_INDEX);
+        kcnt[kb] = good ? e - b : 0;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; s++) {
+            mbar_init(smem_u32(&ms->full[s]), 1);
+            mbar_init(smem_u32(&ms->empty[s]), 1);
+        }
+        for (int w = 0; w < 2; w++) {
+            mbar_init(smem_u32(&ms->q_ready[w]), 1);
+            mbar_init(smem_u32(&ms->s_full[w]), 1);
+            mbar_init(smem_u32(&ms->s_free[w]), 128);
+            mbar_init(smem_u32(&ms->p_full[w]), 128);
+            mbar_init(smem_u32(&ms->p_free[w]), 1);
+            mbar_init(smem_u32(&ms->acc_full[w]), 1);
+            mbar_init(smem_u32(&ms->acc_free[w]), 128);
+        }
+        mbar_init(smem_u32(&ms->drain), 1);
+        ms->abort_flag = 0;
+        fence_mbar_init();
+    }
+    fence_async_smem();
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of the item counts (ceil(count / 8)) over key blocks
+        int carry = 0;
+        for (int base = 0; base < n_kb; base += 32) {
+            const int kb = base + lane;
+            const int v = kb < n_kb ? (kcnt[kb] + 7) / 8 : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            if (kb < n_kb) kitem[kb] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) {
+            ms->n_kb = n_kb;
+            ms->n_items = carry;
+        }
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = ms->tmem_slot;
+    const int n_items = ms->n_items;
+
+    if ((warp == 0 || warp == 2 || warp == 3) && (warp == 0 ? 0 : warp - 1) < C::NPROD) {
+        // ----------------------------------------------------------- gather
+        const int pw = warp == 0 ? 0 : warp - 1;
+        int kb = 0, issued = -1;
+        for (int n = pw; n < n_items; n += C::NPROD) {
+            while (kb + 1 < n_kb && kitem[kb + 1] <= n) kb++;
+            const int gi = n - kitem[kb];
+            const int nv = min(8, kcnt[kb] - 8 * gi);
+            int st, u;
+            stage_of<C>(n, st, u);
+            bool ok = true;
+            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
+            if (!ok) break;
+            const long long g = blockIdx.x + (long long)kb * G;
+            const long long slice = g / a.T;
+            const int j = (int)(g - slice * a.T);
+            const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
+            const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
+            int qb = 0;
+            if (lane < nv) {
+                qb = ri[cp[j] + 8 * gi + lane];
+                if (qb < 0 || qb >= a.T) {
+                    set_status(a.status, LLSA_ERR_BAD_INDEX);
+                    qb = 0;
+                }
+            }
+            unsigned char* sb = stages + st * C::STAGE_BYTES;
+            const uint32_t fb = smem_u32(&ms->full[st]);
+            if (lane == 0) mbar_arrive_expect_tx(fb, nv * (2 * C::KB_BYTES + 128) + 2 * C::KB_BYTES);
+            __syncwarp();
+            if (lane == 0) {
+                const int yk = (int)(slice * a.n + (long long)j * 16);
+                for (int r = 0; r < C::REG; r++) {
+                    tma_load_2d(smem_u32(sb + C::OFF_K + r * 2048), &mk, r * 64, yk, fb);
+                    tma_load_2d(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, yk, fb);
+                }
+            }
+            if (lane < nv) {
+                const long long tok = slice * a.n + (long long)qb * 16;
+                for (int r = 0; r < C::REG; r++) {
+                    tma_load_2d(smem_u32(sb + r * 128 * 128 + lane * 2048), &mq, r * 64, (int)tok, fb);
+                    tma_load_2d(smem_u32(sb + C::OFF_DO + r * 128 * 128 + lane * 2048), &mdo, r * 64, (int)tok, fb);
+                }
+                bulk_load(smem_u32(sb + C::OFF_LD + lane * 128), a.Dbuf + 2 * tok, 128, fb);
+            }
+            issued = n;
+        }
+        if (lane == 0)
+            for (int n = issued; n >= 0 && n > issued - C::NPROD * C::SPP; n -= C::NPROD) {
+                int st, u;
+                stage_of<C>(n, st, u);
+                for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->full[st]), u & 1); it++) {
+                }
+            }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
+            constexpr uint32_t idG = idesc_bf16(D, 16, 1, 0);
+            const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);         // K-major
+            const uint64_t dMN = desc_sw128(smem_u32(stages), 128 * 128, 1024);  // stacks as MN-major
+            const uint64_t dPB = desc_sw128(smem_u32(pbuf), 16, 1024);
+            // Item n belongs to the warpgroup of its key block (kb & 1); k is its
+            // index within that group's items, kn its count of non-empty key
+            // blocks before this one. Per-group barriers see their phases in
+            // that group's order, so no wait can alias an older phase.
+            int wk[2] = {0, 0}, wkb[2] = {0, 0};
+            struct Item { int n, w, k, kn, gi; bool last; };
+            auto issue_S = [&](const Item& it) -> bool {
+                int st, u;
+                stage_of<C>(it.n, st, u);
+                if (!mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status)) return false;
+                if (it.k >= 1 && !mbar_wait(smem_u32(&ms->s_free[it.w]), (it.k - 1) & 1, abort_flag, a.status))
+                    return false;
+                mbar_arrive(smem_u32(&ms->q_ready[it.w]));
+                tc_fence_after();
+                const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ks++) {
+                    const uint32_t qoff = (ks / 4) * 128 * 128 + (ks % 4) * 32;
+                    const uint32_t koff = (ks / 4) * 2048 + (ks % 4) * 32;
+                    mma_bf16(tbase + it.w * 32, dKm + ((s0 + qoff) >> 4), dKm + ((s0 + C::OFF_K + koff) >> 4), idS,
+                             ks > 0);
+                    mma_bf16(tbase + it.w * 32 + 16, dKm + ((s0 + C::OFF_DO + qoff) >> 4),
+                             dKm + ((s0 + C::OFF_V + koff) >> 4), idS, ks > 0);
+                }
+                mma_commit(smem_u32(&ms->s_full[it.w]));
+                return true;
+            };
+            auto issue_G = [&](const Item& it) -> bool {
+                int st, u;
+                stage_of<C>(it.n, st, u);
+                if (!mbar_wait(smem_u32(&ms->p_full[it.w]), it.k & 1, abort_flag, a.status)) return false;
+                // the accumulators are free once the previous key block's epilogue read them
+                if (it.gi == 0 && it.kn >= 1 &&
+                    !mbar_wait(smem_u32(&ms->acc_free[it.w]), (it.kn - 1) & 1, abort_flag, a.status))
+                    return false;
+                tc_fence_after();
+                const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
+                const uint32_t pb = (uint32_t)(it.w * 2 * C::PB_BYTES);
+#pragma unroll
+                for (int ks = 0; ks < 8; ks++) {
+                    const uint32_t boff = pb + (ks / 4) * 2048 + (ks % 4) * 32;
+                    const uint32_t acc = (it.gi > 0 || ks > 0) ? 1u : 0u;
+                    mma_bf16(tbase + 64 + it.w * 32 + 16, dMN + ((s0 + C::OFF_DO + ks * 2048) >> 4), dPB + (boff >> 4),
+                             idG, acc);
+                    mma_bf16(tbase + 64 + it.w * 32, dMN + ((s0 + ks * 2048) >> 4), dPB + ((boff + C::PB_BYTES) >> 4),
+                             idG, acc);
+                }
+                mma_commit(smem_u32(&ms->p_free[it.w]));
+                mma_commit(smem_u32(&ms->empty[st]));
+                if (it.last) mma_commit(smem_u32(&ms->acc_full[it.w]));
+                return true;
+            };
+            int kb = 0;
+            bool ok = true, have_pending = false;
+            Item pending{};
+            for (int n = 0; ok && n < n_items; n++) {
+                while (kb + 1 < n_kb && kitem[kb + 1] <= n) kb++;
+                Item it;
+                it.n = n;
+                it.w = kb & 1;
+                it.gi = n - kitem[kb];
+                it.last = 8 * (it.gi + 1) >= kcnt[kb];
+                it.k = wk[it.w]++;
+                it.kn = wkb[it.w];
+                if (it.last) wkb[it.w]++;
+                // S of this item goes ahead of the previous item's gradient MMAs
+                // when the two belong to different warpgroups
+                if (have_pending && pending.w == it.w) {
+                    ok = issue_G(pending);
+                    have_pending = false;
+                }
+                if (ok) ok = issue_S(it);
+                if (ok && have_pending) ok = issue_G(pending);
+                pending = it;
+                have_pending = true;
+            }
+            if (ok && have_pending) issue_G(pending);
+            mma_commit(smem_u32(&ms->drain));
+            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------ P, dS per query row; epilogue
+        const int w = (warp - 4) >> 2, qr = warp & 3;
+        const int tq = threadIdx.x - 128 * (1 + w);  // query row of the stack = TMEM lane
+        const uint32_t lanes = (uint32_t)(qr * 32) << 16;
+        const float sc = a.scale, scl2 = a.scale * kLog2e;
+        const int dd = D == 64 ? 16 * qr + lane : 32 * qr + lane;
+        const bool valid = D == 64 ? lane < 16 : true;
+        int acc_phase = 0, k = 0;
+        for (int kb = w; kb < n_kb; kb += 2) {
+            const long long g = blockIdx.x + (long long)kb * G;
+            const long long slice = g / a.T;
+            const int j = (int)(g - slice * a.T);
+            const int cnt = kcnt[kb], items = (cnt + 7) / 8;
+            for (int gi = 0; gi < items; gi++, k++) {
+                const int n = kitem[kb] + gi;
+                int st, u;
+                stage_of<C>(n, st, u);
+                const unsigned char* sb = stages + st * C::STAGE_BYTES;
+                const bool row_ok = tq < 16 * min(8, cnt - 8 * gi);
+                // waits return at once after a timeout; the group keeps walking
+                mbar_wait(smem_u32(&ms->q_ready[w]), k & 1, abort_flag, a.status);
+                const float2 ld = *reinterpret_cast<const float2*>(sb + C::OFF_LD + tq * 8);  // (lse, D)
+                const float lse2 = ld.x * kLog2e, Dq = ld.y;
+                mbar_wait(smem_u32(&ms->s_full[w]), k & 1, abort_flag, a.status);
+                tc_fence_after();
+                float s[16], dp[16];
+                tmem_ld16(tbase + lanes + w * 32, s);
+                tmem_ld16(tbase + lanes + w * 32 + 16, dp);
+                tc_fence_before();
+                mbar_arrive(smem_u32(&ms->s_free[w]));
+                // the P / dS operands of this group's previous item must be consumed
+                if (k >= 1) mbar_wait(smem_u32(&ms->p_free[w]), (k - 1) & 1, abort_flag, a.status);
+                unsigned char* PT = pbuf + w * 2 * C::PB_BYTES;
+                unsigned char* pb = PT + (tq >> 6) * 2048 + (tq & 7) * 2;
+                const int chk = (tq & 63) >> 3;
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    float pr = ex2(fmaf(s[c], scl2, -lse2));
+                    float ds = pr * (dp[c] - Dq);
+                    if (!row_ok) {
+                        pr = 0.f;
+                        ds = 0.f;
+                    }
+                    const uint32_t off = c * 128 + ((chk ^ (c & 7)) << 4);
+                    *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pr);
+                    *reinterpret_cast<__nv_bfloat16*>(pb + C::PB_BYTES + off) = __float2bfloat16_rn(ds);
+                }
+                fence_async_smem();
+                mbar_arrive(smem_u32(&ms->p_full[w]));
+            }
+            // epilogue: dk = scale * acc + pooled fold, dv = acc + pooled fold
+            float kk[16], vv[16];
+            if (items > 0) {
+                mbar_wait(smem_u32(&ms->acc_full[w]), acc_phase & 1, abort_flag, a.status);
+                acc_phase++;
+                tc_fence_after();
+                tmem_ld16(tbase + lanes + 64 + w * 32, kk);
+                tmem_ld16(tbase + lanes + 64 + w * 32 + 16, vv);
+                tc_fence_before();
+            } else {
+#pragma unroll
+                for (int c = 0; c < 16; c++) kk[c] = vv[c] = 0.f;
+            }
+            if (valid) {
+                float fk = 0.f, fv = 0.f;
+                long long span = a.B;
+                int anc = j;
+                for (int l = 1; l <= a.Le; l++) {
+                    const long long off = (slice * a.P + a.lv.row_offset[l] + anc) * (long long)D + dd;
+                    const float inv = 1.0f / (float)span;
+                    fk = fmaf(a.dKc[off], inv, fk);
+                    fv = fmaf(a.dVc[off], inv, fv);
+                    span *= a.B;
+                    anc /= a.B;
+                }
+                __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + (slice * a.n + (long long)j * 16) * D + dd;
+                __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + (slice * a.n + (long long)j * 16) * D + dd;
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+                    dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
+                }
+            }
+            if (items > 0) mbar_arrive(smem_u32(&ms->acc_free[w]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 128);
+    }
+}
+
+template <int D>
+int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
+    using C = Cfg<D>;
+    static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(sizeof(Misc) <= 4096, "misc block");
+    // the MMA thread holds one item's gradient MMAs back while it issues the
+    // next item's S; that needs a second stage
+    static_assert(C::STAGES >= 2, "two stages at least");
+    cudaFuncSetAttribute(bwd_dkv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const long long total = s.slices * (long long)s.T;
+    const int grid = (int)std::min<long long>(total, (long long)sm_count());
+    if ((total + grid - 1) / grid > kMaxKeyBlocks) return LLSA_ERR_UNSUPPORTED;
+    LLSA_LAUNCH("bwd_dkv_tc", st,
+                bwd_dkv_tc_kernel<D><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], a));
+    return LLSA_OK;
+}
+
+}  // namespace
+
+bool bwd_dkv_tc_fits(const Shape& s) {
+    const long long total = s.slices * (long long)s.T;
+    const int grid = (int)std::min<long long>(total, (long long)sm_count());
+    return grid > 0 && (total + grid - 1) / grid <= kMaxKeyBlocks;
+}
+
+int launch_bwd_dkv_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
+    CUtensorMap maps[4];
+    const long long rows = s.slices * (long long)s.n;
+    const void* bases[4] = {a.q, a.dout, a.k, a.v};
+    for (int t = 0; t < 4; t++) LLSA_TRY(make_tmap_bf16(&maps[t], bases[t], rows, s.d, 16));
+    return s.d == 64 ? launch_cfg<64>(s, a, maps, st) : launch_cfg<128>(s, a, maps, st);
+}
+
+}  // namespace llsa

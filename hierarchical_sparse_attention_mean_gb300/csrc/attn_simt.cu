@@ -481,7 +481,7 @@ AttnArgs make_attn_args(const Shape& s) {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t bwd_workspace_bytes(const Shape& s) {
-    size_t b = align256(sizeof(float) * s.slices * (size_t)s.n);                       // D
+    size_t b = align256(2 * sizeof(float) * s.slices * (size_t)s.n);                   // D (or (lse, D) pairs)
     b += 2 * align256(sizeof(float) * s.slices * (size_t)s.T * s.Le * s.d);            // gK, gV
     b += 2 * align256(sizeof(float) * s.slices * (size_t)s.P * s.d);                   // dKc, dVc
     return b;
@@ -490,7 +490,7 @@ size_t bwd_workspace_bytes(const Shape& s) {
 void carve_bwd_workspace(const Shape& s, void* ws, AttnArgs* a) {
     char* w = static_cast<char*>(ws);
     a->Dbuf = reinterpret_cast<float*>(w);
-    w += align256(sizeof(float) * s.slices * (size_t)s.n);
+    w += align256(2 * sizeof(float) * s.slices * (size_t)s.n);
     const size_t gsz = align256(sizeof(float) * s.slices * (size_t)s.T * s.Le * s.d);
     a->gK = reinterpret_cast<float*>(w); w += gsz;
     a->gV = reinterpret_cast<float*>(w); w += gsz;
