@@ -42,7 +42,7 @@ struct Cfg {
     static constexpr int OFF_LD = OFF_V + KB_BYTES;
     static constexpr int STAGE_BYTES = OFF_LD + 1024;
     static constexpr int PB_BYTES = 16 * 128 * 2;  // P^T or dS^T of one item
-    static constexpr int FIXED = 4 * PB_BYTES + 4096 + kMaxKeyBlocks * 8;
+    static constexpr int FIXED = 4 * PB_BYTES + 4096 + kMaxKeyBlocks * 12;
     static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
     static constexpr int NPROD = STAGES_RAW >= 3 ? 3 : (STAGES_RAW >= 2 ? 2 : 1);
     static constexpr int SPP = (STAGES_RAW < 1 ? 1 : (STAGES_RAW > 6 ? 6 : STAGES_RAW)) / NPROD;
@@ -77,6 +77,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     Misc* ms = reinterpret_cast<Misc*>(pbuf + 4 * C::PB_BYTES);
     int* kcnt = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(ms) + 4096);  // per key block: column count
     int* kitem = kcnt + kMaxKeyBlocks;                                                  // first item of the key block
+    int* kbeg = kitem + kMaxKeyBlocks;                                                  // first CSC entry of the column
     volatile int* abort_flag = &ms->abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -99,6 +100,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         const bool good = b >= 0 && e >= b && e <= a.K1 * a.T;
         if (!good) set_status(a.status, LLSA_ERR_BAD_INDEX);
         kcnt[kb] = good ? e - b : 0;
+        kbeg[kb] = good ? b : 0;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
@@ -150,11 +152,21 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     if ((warp == 0 || warp == 2 || warp == 3) && (warp == 0 ? 0 : warp - 1) < C::NPROD) {
         // ----------------------------------------------------------- gather
         const int pw = warp == 0 ? 0 : warp - 1;
-        int kb = 0, issued = -1;
+        // the query blocks of the next item are loaded while this one is issued
+        int kb_walk = 0;
+        auto locate = [&](int n, int& kb, int& gi, int& nv, int& qb) {
+            while (kb_walk + 1 < n_kb && kitem[kb_walk + 1] <= n) kb_walk++;
+            kb = kb_walk;
+            gi = n - kitem[kb];
+            nv = min(8, kcnt[kb] - 8 * gi);
+            qb = lane < nv ? a.row_idx[((long long)(blockIdx.x + (long long)kb * G) / a.T) * a.T * a.K1 + kbeg[kb] + 8 * gi + lane] : 0;
+        };
+        int kb, gi, nv, qb, kb1 = 0, gi1 = 0, nv1 = 0, qb1 = 0;
+        int issued = -1;
+        if (pw < n_items) locate(pw, kb1, gi1, nv1, qb1);
         for (int n = pw; n < n_items; n += C::NPROD) {
-            while (kb + 1 < n_kb && kitem[kb + 1] <= n) kb++;
-            const int gi = n - kitem[kb];
-            const int nv = min(8, kcnt[kb] - 8 * gi);
+            kb = kb1; gi = gi1; nv = nv1; qb = qb1;
+            if (n + C::NPROD < n_items) locate(n + C::NPROD, kb1, gi1, nv1, qb1);
             int st, u;
             stage_of<C>(n, st, u);
             bool ok = true;
@@ -164,15 +176,9 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             const long long g = blockIdx.x + (long long)kb * G;
             const long long slice = g / a.T;
             const int j = (int)(g - slice * a.T);
-            const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
-            const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
-            int qb = 0;
-            if (lane < nv) {
-                qb = ri[cp[j] + 8 * gi + lane];
-                if (qb < 0 || qb >= a.T) {
-                    set_status(a.status, LLSA_ERR_BAD_INDEX);
-                    qb = 0;
-                }
+            if (lane < nv && (qb < 0 || qb >= a.T)) {
+                set_status(a.status, LLSA_ERR_BAD_INDEX);
+                qb = 0;
             }
             unsigned char* sb = stages + st * C::STAGE_BYTES;
             const uint32_t fb = smem_u32(&ms->full[st]);
@@ -306,6 +312,20 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             const long long slice = g / a.T;
             const int j = (int)(g - slice * a.T);
             const int cnt = kcnt[kb], items = (cnt + 7) / 8;
+            // pooled-level gradients above this key block, fetched before its items
+            float fk = 0.f, fv = 0.f;
+            if (valid) {
+                long long span = a.B;
+                int anc = j;
+                for (int l = 1; l <= a.Le; l++) {
+                    const long long off = (slice * a.P + a.lv.row_offset[l] + anc) * (long long)D + dd;
+                    const float inv = 1.0f / (float)span;
+                    fk = fmaf(a.dKc[off], inv, fk);
+                    fv = fmaf(a.dVc[off], inv, fv);
+                    span *= a.B;
+                    anc /= a.B;
+                }
+            }
             for (int gi = 0; gi < items; gi++, k++) {
                 const int n = kitem[kb] + gi;
                 int st, u;
@@ -357,17 +377,6 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 for (int c = 0; c < 16; c++) kk[c] = vv[c] = 0.f;
             }
             if (valid) {
-                float fk = 0.f, fv = 0.f;
-                long long span = a.B;
-                int anc = j;
-                for (int l = 1; l <= a.Le; l++) {
-                    const long long off = (slice * a.P + a.lv.row_offset[l] + anc) * (long long)D + dd;
-                    const float inv = 1.0f / (float)span;
-                    fk = fmaf(a.dKc[off], inv, fk);
-                    fv = fmaf(a.dVc[off], inv, fv);
-                    span *= a.B;
-                    anc /= a.B;
-                }
                 __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + (slice * a.n + (long long)j * 16) * D + dd;
                 __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + (slice * a.n + (long long)j * 16) * D + dd;
 #pragma unroll

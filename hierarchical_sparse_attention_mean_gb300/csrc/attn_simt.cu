@@ -415,32 +415,90 @@ void allow_smem(K kernel, size_t smem) {
 
 // Gradient of every pooled token used by enrichment: the sum, in ascending
 // query-block order, of the coarse partials of the query blocks that used it.
-// Level 1 tokens are fine blocks that their users also selected (TOP1 picks
-// from the selection), so the fine CSC column lists the candidates; level
-// l >= 2 tokens scan the level's ancestors (one rank-1 token per ancestor).
-__global__ void __launch_bounds__(64) coarse_reduce_kernel(AttnArgs a) {
+// One warp per pooled row. Level-1 tokens are fine blocks their users also
+// selected (TOP1 picks from the selection), so the fine CSC column lists the
+// candidates; level l >= 2 tokens scan the level's ancestors (one rank-1 token
+// per ancestor, shared by its B^(l-1) query blocks). Candidates are tested 32
+// at a time (one per lane), the hits compacted in lane order, and their rows
+// summed in that order with several rows in flight; each lane owns kCols
+// consecutive columns.
+constexpr int kReduceWarps = 8;
+
+template <int kCols>
+__device__ __forceinline__ void load_cols(const float* p, bool ok, float (&v)[kCols]) {
+    if (!ok) {
+#pragma unroll
+        for (int c = 0; c < kCols; c++) v[c] = 0.f;
+    } else if constexpr (kCols == 1) {
+        v[0] = *p;
+    } else if constexpr (kCols == 2) {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        v[0] = t.x; v[1] = t.y;
+    } else {
+#pragma unroll
+        for (int c = 0; c < kCols; c += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(p + c);
+            v[c] = t.x; v[c + 1] = t.y; v[c + 2] = t.z; v[c + 3] = t.w;
+        }
+    }
+}
+
+template <int kCols>  // columns per lane: d <= 32 * kCols, d % kCols == 0
+__global__ void __launch_bounds__(32 * kReduceWarps) coarse_reduce_kernel(AttnArgs a, int rows) {
+    constexpr int kUnroll = kCols >= 8 ? 2 : 16 / kCols;  // rows in flight
+    __shared__ int hits[kReduceWarps][32];
     const long long slice = blockIdx.y;
-    const int row = blockIdx.x;  // pyramid row over levels 1..Le
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // pyramid row over levels 1..Le, coarsest first: a row of level l sums
+    // B^(l-1) partial rows per hit, so the long ones start in the first wave
+    const int row = rows - 1 - (int)(blockIdx.x * kReduceWarps + warp);
+    if (row < 0) return;
     int l = 1;
     while (l < a.Le && row >= a.lv.row_offset[l + 1]) l++;
     const int e = row - a.lv.row_offset[l];
-    const int d = a.d, C4 = d / 4, tid = threadIdx.x, lane = tid & 31;
-    const bool active = tid < C4;
-    float4 ak = make_float4(0.f, 0.f, 0.f, 0.f), av = ak;
-    auto add = [&](int i) {
-        if (!active) return;
-        const long long off = ((slice * a.T + i) * a.Le + (l - 1)) * (long long)d + tid * 4;
-        const float4 k4 = *reinterpret_cast<const float4*>(a.gK + off);
-        const float4 v4 = *reinterpret_cast<const float4*>(a.gV + off);
-        ak.x += k4.x; ak.y += k4.y; ak.z += k4.z; ak.w += k4.w;
-        av.x += v4.x; av.y += v4.y; av.z += v4.z; av.w += v4.w;
+    const int d = a.d;
+    const bool active = lane * kCols < d;
+    const long long rstride = (long long)a.Le * d;  // between consecutive query blocks
+    const long long base = (slice * a.T * a.Le + (l - 1)) * (long long)d + lane * kCols;
+    const float* gk = a.gK + base;
+    const float* gv = a.gV + base;
+    float ak[kCols], av[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; c++) ak[c] = av[c] = 0.f;
+    // rows src(0..count-1), kUnroll loads in flight, added in order
+    auto add_rows = [&](int count, auto src) {
+        for (int r0 = 0; r0 < count; r0 += kUnroll) {
+            float pk[kUnroll][kCols], pv[kUnroll][kCols];
+#pragma unroll
+            for (int u = 0; u < kUnroll; u++) {
+                const bool ok = active && r0 + u < count;
+                const long long off = ok ? (long long)src(r0 + u) * rstride : 0;
+                load_cols<kCols>(gk + off, ok, pk[u]);
+                load_cols<kCols>(gv + off, ok, pv[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; u++)
+#pragma unroll
+                for (int c = 0; c < kCols; c++) {
+                    ak[c] += pk[u][c];
+                    av[c] += pv[u][c];
+                }
+        }
     };
+    int* h = hits[warp];
     if (l == 1) {
         const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
         const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
-        for (int x = cp[e]; x < cp[e + 1]; x++) {
-            const int i = ri[x];
-            if (i >= 0 && i < a.T && a.coarse[(slice * a.T + i) * a.L] == e) add(i);
+        const int beg = cp[e], end = cp[e + 1];
+        for (int x0 = beg; x0 < end; x0 += 32) {
+            const int x = x0 + lane;
+            const int i = x < end ? ri[x] : -1;
+            const bool hit = i >= 0 && i < a.T && a.coarse[(slice * a.T + i) * a.L] == e;
+            const unsigned bits = __ballot_sync(0xffffffffu, hit);
+            if (hit) h[__popc(bits & ((1u << lane) - 1u))] = i;
+            __syncwarp();
+            add_rows(__popc(bits), [&](int r) { return h[r]; });
+            __syncwarp();
         }
     } else {
         int span = 1;
@@ -449,19 +507,24 @@ __global__ void __launch_bounds__(64) coarse_reduce_kernel(AttnArgs a) {
         for (int a0 = 0; a0 < nl; a0 += 32) {
             const int anc = a0 + lane;
             const bool hit = anc < nl && a.coarse[(slice * a.T + (long long)anc * span) * a.L + (l - 1)] == e;
-            unsigned bits = __ballot_sync(0xffffffffu, hit);
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1;
-                const int first = (a0 + b) * span;
-                for (int i = first; i < first + span; i++) add(i);
+            const unsigned bits = __ballot_sync(0xffffffffu, hit);
+            if (hit) h[__popc(bits & ((1u << lane) - 1u))] = anc;
+            __syncwarp();
+            const int cnt = __popc(bits);
+            for (int j = 0; j < cnt; j++) {
+                const int first = h[j] * span;
+                add_rows(span, [&](int r) { return first + r; });
             }
+            __syncwarp();
         }
     }
     if (active) {
-        const long long off = (slice * a.P + a.lv.row_offset[l] + e) * (long long)d + tid * 4;
-        *reinterpret_cast<float4*>(a.dKc + off) = ak;
-        *reinterpret_cast<float4*>(a.dVc + off) = av;
+        const long long out = (slice * a.P + a.lv.row_offset[l] + e) * (long long)d + lane * kCols;
+#pragma unroll
+        for (int c = 0; c < kCols; c++) {
+            a.dKc[out + c] = ak[c];
+            a.dVc[out + c] = av[c];
+        }
     }
 }
 
@@ -503,7 +566,16 @@ int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     if (s.Le == 0) return LLSA_OK;
     int rows = 0;
     for (int l = 1; l <= s.Le; l++) rows += s.n_level[l];
-    LLSA_LAUNCH("coarse_reduce", st, coarse_reduce_kernel<<<dim3(rows, (unsigned)s.slices), 64, 0, st>>>(a));
+    const int gx = (rows + kReduceWarps - 1) / kReduceWarps;
+    const dim3 grid(gx, (unsigned)s.slices);
+    if (s.d <= 32)
+        LLSA_LAUNCH("coarse_reduce", st, coarse_reduce_kernel<1><<<grid, 32 * kReduceWarps, 0, st>>>(a, rows));
+    else if (s.d <= 64)
+        LLSA_LAUNCH("coarse_reduce", st, coarse_reduce_kernel<2><<<grid, 32 * kReduceWarps, 0, st>>>(a, rows));
+    else if (s.d <= 128)
+        LLSA_LAUNCH("coarse_reduce", st, coarse_reduce_kernel<4><<<grid, 32 * kReduceWarps, 0, st>>>(a, rows));
+    else
+        LLSA_LAUNCH("coarse_reduce", st, coarse_reduce_kernel<8><<<grid, 32 * kReduceWarps, 0, st>>>(a, rows));
     return LLSA_OK;
 }
 

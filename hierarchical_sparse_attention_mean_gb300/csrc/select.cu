@@ -11,11 +11,14 @@
 //
 // One launch per level, coarsest first (each level needs the one above). A CTA
 // owns up to 16 sibling query rows that share one candidate list: candidate
-// key rows are staged through shared memory in tiles (coalesced float4 loads),
-// each warp scores one query row against the tile, and the warp then runs K
-// rounds of a shuffle arg-max tournament over its row's candidates (each lane
-// holding ceil(C/32) of them). K <= 64 and C <= 1024 here, so K tournament
-// rounds cost less than a full bitonic sort of the C candidates.
+// key rows are staged through shared memory in tiles of 32*KPL (coalesced
+// float4 loads), each warp scores one query row against the tile (a lane owns
+// KPL candidates; packed two-wide fp32 FMAs over even/odd columns), and the
+// warp then runs K rounds of an arg-max tournament over its row's candidates
+// (each lane holding ceil(C/32) of them): scores map to order-preserving
+// unsigned keys, so a round is one warp max-reduction of the key and one
+// min-reduction of the index among the lanes holding that key. K <= 64 and
+// C <= 1024 here, so K rounds cost less than a full sort of the C candidates.
 #include <limits.h>
 
 #include "internal.h"
@@ -23,7 +26,6 @@
 namespace llsa {
 namespace {
 
-constexpr int kTile = 64;     // candidate rows per shared-memory tile
 constexpr int kMaxRows = 16;  // query rows (warps) per CTA
 constexpr int kMaxCand = 1024;
 constexpr int kMaxKeep = 64;
@@ -52,8 +54,17 @@ __device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
     return sa > sb || (sa == sb && ia < ib);
 }
 
-template <int CPL>
+// Order-preserving map of a float to an unsigned key (for non-NaN inputs;
+// -0 and +0 map to the same key).
+__device__ __forceinline__ unsigned order_key(float v) {
+    if (v == 0.f) v = 0.f;
+    const unsigned u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <int CPL, int KPL>
 __global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs a) {
+    constexpr int kTile = 32 * KPL;  // candidate rows per shared-memory tile
     extern __shared__ float4 smem4[];
     const int d = a.d, C = a.C;
     const int ktile_stride = d + 4;
@@ -104,58 +115,56 @@ __global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs 
         __syncthreads();
         if (warp < nrows) {
             const float* qr = qrows + warp * d;
-            float acc0 = 0.f, acc1 = 0.f;
-            const float* k0 = ktile + lane * ktile_stride;
-            const float* k1 = ktile + (lane + 32) * ktile_stride;
+            float2 acc[KPL];
+#pragma unroll
+            for (int j = 0; j < KPL; j++) acc[j] = make_float2(0.f, 0.f);
             for (int c = 0; c < d; c += 4) {
-                float4 q4 = *reinterpret_cast<const float4*>(qr + c);
-                float4 a4 = *reinterpret_cast<const float4*>(k0 + c);
-                float4 b4 = *reinterpret_cast<const float4*>(k1 + c);
-                acc0 = fmaf(q4.x, a4.x, acc0); acc0 = fmaf(q4.y, a4.y, acc0);
-                acc0 = fmaf(q4.z, a4.z, acc0); acc0 = fmaf(q4.w, a4.w, acc0);
-                acc1 = fmaf(q4.x, b4.x, acc1); acc1 = fmaf(q4.y, b4.y, acc1);
-                acc1 = fmaf(q4.z, b4.z, acc1); acc1 = fmaf(q4.w, b4.w, acc1);
+                const float4 q4 = *reinterpret_cast<const float4*>(qr + c);
+                const float2 qa = make_float2(q4.x, q4.y), qb = make_float2(q4.z, q4.w);
+#pragma unroll
+                for (int j = 0; j < KPL; j++) {
+                    const float4 k4 = *reinterpret_cast<const float4*>(ktile + (lane + 32 * j) * ktile_stride + c);
+                    acc[j] = __ffma2_rn(qa, make_float2(k4.x, k4.y), acc[j]);
+                    acc[j] = __ffma2_rn(qb, make_float2(k4.z, k4.w), acc[j]);
+                }
             }
-            if (lane < tn) scores[warp * C + t0 + lane] = acc0;
-            if (lane + 32 < tn) scores[warp * C + t0 + lane + 32] = acc1;
+#pragma unroll
+            for (int j = 0; j < KPL; j++)
+                if (lane + 32 * j < tn) scores[warp * C + t0 + lane + 32 * j] = acc[j].x + acc[j].y;
         }
     }
     __syncthreads();
     if (warp >= nrows) return;
 
-    // Top-K tournament for row `warp`
-    float s[CPL];
+    // Top-K rounds for row `warp`; a NaN score ranks with -inf
+    unsigned key[CPL];
     int idx[CPL];
 #pragma unroll
     for (int m = 0; m < CPL; m++) {
         const int c = lane + 32 * m;
         if (c < C) {
-            float v = scores[warp * C + c];
-            s[m] = (v != v) ? -INFINITY : v;  // NaN never wins
+            const float v = scores[warp * C + c];
+            key[m] = order_key(v != v ? -INFINITY : v);
             idx[m] = cand[c];
         } else {
-            s[m] = -INFINITY;
+            key[m] = 0u;  // below every score
             idx[m] = INT_MAX;
         }
     }
     unsigned taken = 0;
     int* krow = kept + warp * kMaxKeep;
     for (int k = 0; k < a.Kl; k++) {
-        float bs = -INFINITY;
+        unsigned bk = 0u;
         int bi = INT_MAX;
 #pragma unroll
         for (int m = 0; m < CPL; m++)
-            if (!(taken >> m & 1u) && better(s[m], idx[m], bs, bi)) { bs = s[m]; bi = idx[m]; }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (better(os, oi, bs, bi)) { bs = os; bi = oi; }
-        }
+            if (!(taken >> m & 1u) && (key[m] > bk || (key[m] == bk && idx[m] < bi))) { bk = key[m]; bi = idx[m]; }
+        const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
+        const int wi = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bi : 0xffffffffu);
 #pragma unroll
         for (int m = 0; m < CPL; m++)
-            if (idx[m] == bi) taken |= 1u << m;
-        if (lane == 0) krow[k] = bi;
+            if (idx[m] == wi) taken |= 1u << m;
+        if (lane == 0) krow[k] = wi;
     }
     __syncwarp();
     const int row = row0 + warp;
@@ -172,17 +181,30 @@ __global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs 
     for (int q = lane; q < a.span; q += 32) crow[(long long)q * a.L] = top1;
 }
 
-template <int CPL>
-int launch_level(const SelectArgs& a, long long slices, cudaStream_t st) {
+template <int CPL, int KPL>
+size_t level_smem(const SelectArgs& a) {
+    return sizeof(float) * (32 * KPL * (a.d + 4) + kMaxRows * a.d + kMaxRows * a.C) +
+           sizeof(int) * (a.C + kMaxRows * kMaxKeep);
+}
+
+template <int CPL, int KPL>
+int launch_level_kpl(const SelectArgs& a, long long slices, cudaStream_t st) {
     const int grid_x = (a.n_l + a.rows_per_cta - 1) / a.rows_per_cta;
-    const size_t smem = sizeof(float) * (kTile * (a.d + 4) + kMaxRows * a.d + kMaxRows * a.C) +
-                        sizeof(int) * (a.C + kMaxRows * kMaxKeep);
+    const size_t smem = level_smem<CPL, KPL>(a);
     if (smem > 200 * 1024 || slices > 65535) return LLSA_ERR_UNSUPPORTED;
     if (smem > 48 * 1024)
-        cudaFuncSetAttribute(select_level_kernel<CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(select_level_kernel<CPL, KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     LLSA_LAUNCH("select_level", st,
-                select_level_kernel<CPL><<<dim3(grid_x, (unsigned)slices), 32 * a.rows_per_cta, smem, st>>>(a));
+                select_level_kernel<CPL, KPL>
+                <<<dim3(grid_x, (unsigned)slices), 32 * a.rows_per_cta, smem, st>>>(a));
     return LLSA_OK;
+}
+
+// four candidates per lane per tile where the tile fits, else two
+template <int CPL>
+int launch_level(const SelectArgs& a, long long slices, cudaStream_t st) {
+    if (level_smem<CPL, 4>(a) <= 200 * 1024) return launch_level_kpl<CPL, 4>(a, slices, st);
+    return launch_level_kpl<CPL, 2>(a, slices, st);
 }
 
 }  // namespace
