@@ -71,7 +71,9 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, AttnArgs a) {
     using C = Cfg<D>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base (128-byte swizzle atoms), derived from the
+    // __shared__ array by pointer arithmetic so accesses stay shared-space
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stages = sm;
     unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;  // [warpgroup][P^T, dS^T]
     Misc* ms = reinterpret_cast<Misc*>(pbuf + 4 * C::PB_BYTES);

@@ -82,7 +82,9 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                  const __grid_constant__ CUtensorMap mv, AttnArgs a) {
     using C = Cfg<D, NT>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base (128-byte swizzle atoms), derived from the
+    // __shared__ array by pointer arithmetic so accesses stay shared-space
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stages = sm;
     unsigned char* dsbuf = stages + C::STAGES * C::STAGE_BYTES;
     Misc* ms = reinterpret_cast<Misc*>(dsbuf + 2 * C::DS_BYTES);

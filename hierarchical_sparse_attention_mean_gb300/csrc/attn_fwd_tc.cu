@@ -85,7 +85,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
               const __grid_constant__ CUtensorMap mv, AttnArgs a) {
     using C = Cfg<D, NT>;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base (128-byte swizzle atoms), derived from the
+    // __shared__ array by pointer arithmetic so accesses stay shared-space
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stages = sm;
     unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;
     Misc* ms = reinterpret_cast<Misc*>(pbuf + 2 * C::P_BYTES);
@@ -435,6 +437,507 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined variant, used where shared memory holds at least four stages.
+//
+// Differences from the kernel above:
+//  * S^T of a block is issued up to LA blocks ahead of its P V, into one of
+//    two S buffers per group; P and O are double-buffered per group as well,
+//    so a group writes P of its block j and then finishes the epilogue of
+//    block j-1 while P V of j runs on the tensor cores;
+//  * softmax shift: the exponentials subtract the largest pooled-key logit of
+//    the query (computed one block ahead, so it is ready with S) instead of
+//    the row maximum. Softmax is shift-invariant, so only the range matters:
+//    if any fine logit exceeds that shift by more than 2^kShiftSlack, the
+//    group redoes the block with the exact row maximum (S stays in TMEM until
+//    that decision). The common path has one group barrier per block;
+//  * the three gather warps split every block's copies (a warp's copy
+//    requests issue one after another), each arriving on the stage barrier
+//    with its own byte count;
+//  * the MMA warp issues out of order between the S and P V streams (P V
+//    first, as it frees a stage), through an election inside the MMA asm so
+//    that no divergent branch surrounds the MMA instructions.
+constexpr float kShiftSlack = 64.f;  // base-2 exponent range above the shift
+
+template <int D, int NT>
+struct PCfg {
+    static constexpr int NF = NT * 128;
+    static constexpr int REG = D / 64;
+    static constexpr int Q_BYTES = 16 * D * 2;
+    static constexpr int KV_BYTES = NF * D * 2;
+    static constexpr int CO_BYTES = 2 * 4 * D * 4;
+    static constexpr int STAGE_BYTES = Q_BYTES + 2 * KV_BYTES + CO_BYTES;
+    static constexpr int P_BYTES = 16 * NF * 2;
+    static constexpr int FIXED = 4 * P_BYTES + 8192;
+    static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+    static constexpr int LA = STAGES - 1 > 4 ? 4 : STAGES - 1;  // S issued ahead of P V
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
+    static constexpr int TM_S = NT * 16;                         // columns of one S buffer
+    static constexpr int TM_GROUP = 2 * TM_S + 2 * 16;           // two S and two O buffers
+    static constexpr int TM_ALLOC = 2 * TM_GROUP <= 128 ? 128 : 256;
+};
+
+// the stage count of PCfg without instantiating it
+template <int D, int NT>
+constexpr bool pipe_fits() {
+    return (kSmemBudget - (4 * 16 * NT * 128 * 2 + 8192)) / (16 * D * 2 + 2 * NT * 128 * D * 2 + 2 * 4 * D * 4) >= 4;
+}
+
+struct PMisc {
+    float red_sum[2][2][16][4];  // [group][buffer][query][warp]
+    float red_max[2][16][4];     // exact-maximum pass
+    float cmax[2][3][16];        // [group][coarse buffer][query]: largest pooled logit (base 2)
+    float csum[2][3][16];        // sum over levels of 2^(pooled logit - cmax)
+    float cs2[2][3][16][4];      // pooled logits (base 2), -inf beyond L_e
+    float ecs[2][2][16][4];      // coarse probabilities, read by the epilogue
+    float izs[2][2][16];         // 1 / row sum, read by the epilogue
+    int flags[2][2][4];          // per warp: a logit left the shift's range
+    uint64_t full[8], empty[8];
+    uint64_t s_full[2][2], s_free[2][2], p_full[2][2], o_full[2][2], o_free[2][2], drain;
+    uint32_t tmem_slot;
+    int abort_flag;
+};
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, AttnArgs a) {
+    using C = PCfg<D, NT>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* stages = sm;
+    unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;
+    PMisc* ms = reinterpret_cast<PMisc*>(pbuf + 4 * C::P_BYTES);
+    volatile int* abort_flag = &ms->abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long total = a.slices * (long long)a.T;
+    const int G = gridDim.x;
+    const int K1 = NT * 8, Le = a.Le;
+    const long long mine = total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; s++) {
+            mbar_init(smem_u32(&ms->full[s]), 3);  // one arrival per gather warp
+            mbar_init(smem_u32(&ms->empty[s]), 1);
+        }
+        for (int w = 0; w < 2; w++)
+            for (int b = 0; b < 2; b++) {
+                mbar_init(smem_u32(&ms->s_full[w][b]), 1);
+                mbar_init(smem_u32(&ms->s_free[w][b]), 128);
+                mbar_init(smem_u32(&ms->p_full[w][b]), 128);
+                mbar_init(smem_u32(&ms->o_full[w][b]), 1);
+                mbar_init(smem_u32(&ms->o_free[w][b]), 128);
+            }
+        mbar_init(smem_u32(&ms->drain), 1);
+        ms->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), C::TM_ALLOC);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = ms->tmem_slot;
+
+    if (warp == 0 || warp == 2 || warp == 3) {
+        // ----------------------------------------------------------- gather
+        // Block bl uses stage bl % STAGES for the (bl / STAGES)-th time. The
+        // three gather warps split every block's copies (a warp issues its
+        // copies one request at a time): warp 0 the Q block and the K_1 K
+        // blocks, warp 2 the V blocks, warp 3 the pooled K/V rows; each
+        // arrives on the stage barrier with the bytes of its own copies.
+        // Index rows are loaded two blocks ahead.
+        const int role = warp == 0 ? 0 : warp - 1;
+        auto load_idx = [&](long long bl) -> int {
+            if (bl >= mine) return 0;
+            const long long g = blockIdx.x + bl * G;
+            const long long slice = g / a.T;
+            const int i = (int)(g - slice * a.T);
+            if (role < 2) return lane < K1 ? a.sel[(slice * a.T + i) * a.K1 + lane] : 0;
+            return lane < Le ? a.coarse[(slice * a.T + i) * a.L + lane] : 0;
+        };
+        const uint32_t my_bytes = role == 0 ? C::Q_BYTES + C::KV_BYTES : role == 1 ? C::KV_BYTES : 2 * Le * D * 4;
+        int ix0 = load_idx(0), ix1 = load_idx(1);
+        long long issued = -1;
+        for (long long bl = 0; bl < mine; bl++) {
+            int ix = ix0;
+            ix0 = ix1;
+            ix1 = load_idx(bl + 2);
+            const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
+            bool ok = true;
+            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
+            if (!ok) break;
+            const long long g = blockIdx.x + bl * G;
+            const long long slice = g / a.T;
+            const int i = (int)(g - slice * a.T);
+            unsigned char* sQ = stages + st * C::STAGE_BYTES;
+            unsigned char* sK = sQ + C::Q_BYTES;
+            unsigned char* sV = sK + C::KV_BYTES;
+            unsigned char* sC = sV + C::KV_BYTES;
+            const uint32_t fb = smem_u32(&ms->full[st]);
+            if (lane == 0) mbar_arrive_expect_tx(fb, my_bytes);
+            __syncwarp();
+            if (role == 0 && lane == 0) {
+                const int yq = (int)(slice * a.n + (long long)i * 16);
+                for (int r = 0; r < C::REG; r++) tma_load_2d(smem_u32(sQ + r * 16 * 128), &mq, r * 64, yq, fb);
+            }
+            if (role < 2 && lane < K1) {
+                if (ix < 0 || ix >= a.T) {
+                    set_status(a.status, LLSA_ERR_BAD_INDEX);
+                    ix = 0;
+                }
+                const int yk = (int)(slice * a.n + (long long)ix * 16);
+                for (int r = 0; r < C::REG; r++) {
+                    if (role == 0) tma_load_2d(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
+                    else tma_load_2d(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                }
+            }
+            if (role == 2 && lane < Le) {
+                if (ix < 0 || ix >= a.lv.n_level[lane + 1]) {
+                    set_status(a.status, LLSA_ERR_BAD_INDEX);
+                    ix = 0;
+                }
+                const long long row = slice * a.pyr_stride + (long long)(a.lv.row_offset[lane + 1] + ix) * D;
+                bulk_load(smem_u32(sC + lane * D * 4), a.kpyr + row, D * 4, fb);
+                bulk_load(smem_u32(sC + (4 + lane) * D * 4), a.vpyr + row, D * 4, fb);
+            }
+            issued = bl;
+        }
+        // copies still in flight must land before the CTA exits
+        if (lane == 0)
+            for (long long bl = issued; bl >= 0 && bl > issued - C::STAGES; bl--) {
+                const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
+                for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->full[st]), u & 1); it++) {
+                }
+            }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
+        constexpr uint32_t idPV = idesc_bf16(D, 16, 1, 0);
+        const uint64_t dKQ = desc_sw128(smem_u32(stages), 16, 1024);          // K-major
+        const uint64_t dV = desc_sw128(smem_u32(stages), C::NF * 128, 1024);  // MN-major V
+        const uint64_t dP = desc_sw128(smem_u32(pbuf), 16, 1024);
+        // block bl: group bl & 1, its j-th block, buffer j & 1 used for the (j >> 1)-th time
+        auto s_ready = [&](long long bl) -> bool {
+            const int w = (int)(bl & 1), b = (int)((bl >> 1) & 1);
+            const uint32_t use = (uint32_t)(bl >> 2);
+            const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
+            return mbar_test(smem_u32(&ms->full[st]), u & 1) &&
+                   (use == 0 || mbar_test(smem_u32(&ms->s_free[w][b]), (use - 1) & 1));
+        };
+        auto pv_ready = [&](long long bl) -> bool {
+            const int w = (int)(bl & 1), b = (int)((bl >> 1) & 1);
+            const uint32_t use = (uint32_t)(bl >> 2);
+            return mbar_test(smem_u32(&ms->p_full[w][b]), use & 1) &&
+                   (use == 0 || mbar_test(smem_u32(&ms->o_free[w][b]), (use - 1) & 1));
+        };
+        auto issue_S = [&](long long bl) {
+            const int w = (int)(bl & 1), b = (int)((bl >> 1) & 1);
+            const int st = (int)(bl % C::STAGES);
+            tc_fence_after();
+            const uint32_t q0 = (uint32_t)(st * C::STAGE_BYTES), k0 = q0 + C::Q_BYTES;
+            const uint32_t dt = tbase + w * C::TM_GROUP + b * C::TM_S;
+#pragma unroll
+            for (int t = 0; t < NT; t++)
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ks++) {
+                    const uint64_t da = dKQ + ((k0 + (ks / 4) * C::NF * 128 + t * 128 * 128 + (ks % 4) * 32) >> 4);
+                    const uint64_t db = dKQ + ((q0 + (ks / 4) * 16 * 128 + (ks % 4) * 32) >> 4);
+                    mma_bf16_warp(dt + t * 16, da, db, idS, ks > 0);
+                }
+            mma_commit_warp(smem_u32(&ms->s_full[w][b]));
+        };
+        auto issue_PV = [&](long long bl) {
+            const int w = (int)(bl & 1), b = (int)((bl >> 1) & 1);
+            const int st = (int)(bl % C::STAGES);
+            tc_fence_after();
+            const uint32_t v0 = (uint32_t)(st * C::STAGE_BYTES + C::Q_BYTES + C::KV_BYTES);
+            const uint32_t p0 = (uint32_t)((w * 2 + b) * C::P_BYTES);
+            const uint32_t dt = tbase + w * C::TM_GROUP + 2 * C::TM_S + b * 16;
+#pragma unroll
+            for (int ks = 0; ks < C::NF / 16; ks++) {
+                const uint64_t da = dV + ((v0 + ks * 2048) >> 4);
+                const uint64_t db = dP + ((p0 + (ks / 4) * 2048 + (ks % 4) * 32) >> 4);
+                mma_bf16_warp(dt, da, db, idPV, ks > 0);
+            }
+            mma_commit_warp(smem_u32(&ms->o_full[w][b]));
+            mma_commit_warp(smem_u32(&ms->empty[st]));
+        };
+        // Out-of-order issue between the two in-order streams: P V of the
+        // oldest block as soon as its P is written (it frees a stage), else
+        // S of the next block once its operands have landed, at most LA
+        // blocks ahead of P V. Idle polls are bounded like every other wait.
+        long long nS = 0, nP = 0;
+        int idle = 0;
+        while (nP < mine) {
+            int act = 0;
+            if (lane == 0) {
+                if (nP < nS && pv_ready(nP)) act = 2;
+                else if (nS < mine && nS < nP + C::LA && s_ready(nS)) act = 1;
+            }
+            act = __shfl_sync(0xffffffffu, act, 0);
+            if (act == 1) {
+                issue_S(nS++);
+                idle = 0;
+            } else if (act == 2) {
+                issue_PV(nP++);
+                idle = 0;
+            } else {
+                int stop = 0;
+                if (lane == 0) {
+                    if (++idle >= kSpinLimit) {
+                        *abort_flag = 1;
+                        set_status(a.status, LLSA_ERR_TIMEOUT);
+                        stop = 1;
+                    } else if ((idle & 63) == 0 && *abort_flag) {
+                        stop = 1;
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            }
+        }
+        // no MMA may be in flight when TMEM is released
+        mma_commit_warp(smem_u32(&ms->drain));
+        if (lane == 0)
+            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+            }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ----------------------------------------- softmax + epilogue groups
+        const int w = (warp - 4) >> 2, qr = warp & 3;
+        const int tw = threadIdx.x - 128 * (1 + w);
+        const uint32_t lanes = (uint32_t)(qr * 32) << 16;
+        const float sc = a.scale, scl2 = a.scale * kLog2e;
+        const int dd = D == 64 ? 16 * qr + lane : 32 * qr + lane;  // O^T row this thread reads back
+        const bool valid = D == 64 ? lane < 16 : true;
+        const long long nblk = mine > w ? (mine - w + 1) / 2 : 0;  // blocks w, w + 2, ...
+        const int cq = tw >> 3, cpart = tw & 7;                   // pooled-score role
+        // pooled-key logits (base 2, + l ln B) of the group's block j into coarse buffer cb;
+        // eight threads per query, each a 16-byte chunk of the row per 64 columns
+        auto coarse = [&](long long j, int cb) {
+            const long long bl = w + 2 * j;
+            const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
+            mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status);
+            const unsigned char* sQ = stages + st * C::STAGE_BYTES;
+            const float* sCk = reinterpret_cast<const float*>(sQ + C::Q_BYTES + 2 * C::KV_BYTES);
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cc = 0; cc < D / 64; cc++) {
+                const int c8 = cpart + 8 * cc;
+                const uint4 raw = *reinterpret_cast<const uint4*>(sQ + sw128_offset(cq, c8 * 8, 16));
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                const float2 x0 = __bfloat1622float2(h[0]), x1 = __bfloat1622float2(h[1]);
+                const float2 x2 = __bfloat1622float2(h[2]), x3 = __bfloat1622float2(h[3]);
+#pragma unroll
+                for (int l = 0; l < 4; l++)
+                    if (l < Le) {
+                        const float4 k0 = *reinterpret_cast<const float4*>(sCk + l * D + c8 * 8);
+                        const float4 k1 = *reinterpret_cast<const float4*>(sCk + l * D + c8 * 8 + 4);
+                        float t0 = x0.x * k0.x, t1 = x0.y * k0.y;
+                        t0 = fmaf(x1.x, k0.z, t0); t1 = fmaf(x1.y, k0.w, t1);
+                        t0 = fmaf(x2.x, k1.x, t0); t1 = fmaf(x2.y, k1.y, t1);
+                        t0 = fmaf(x3.x, k1.z, t0); t1 = fmaf(x3.y, k1.w, t1);
+                        acc[l] += t0 + t1;
+                    }
+            }
+            float cs[4], cm = -INFINITY;
+#pragma unroll
+            for (int l = 0; l < 4; l++) {
+                float v = acc[l];
+                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                cs[l] = l < Le ? (sc * v + (float)(l + 1) * a.lnB) * kLog2e : -INFINITY;
+                cm = fmaxf(cm, cs[l]);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int l = 0; l < 4; l++)
+                if (l < Le) sum += ex2(cs[l] - cm);
+            if (cpart == 0) {
+                ms->cmax[w][cb][cq] = cm;
+                ms->csum[w][cb][cq] = sum;
+            }
+            if (cpart < 4) ms->cs2[w][cb][cq][cpart] = cpart == 0 ? cs[0] : cpart == 1 ? cs[1] : cpart == 2 ? cs[2] : cs[3];
+        };
+        auto epilogue = [&](long long j, const float* vcp) {
+            const long long bl = w + 2 * j;
+            const int b = (int)(j & 1);
+            const uint32_t use = (uint32_t)(j >> 1);
+            const long long g = blockIdx.x + bl * G;
+            const long long slice = g / a.T;
+            const int i = (int)(g - slice * a.T);
+            mbar_wait(smem_u32(&ms->o_full[w][b]), use & 1, abort_flag, a.status);
+            tc_fence_after();
+            float o[16];
+            tmem_ld16(tbase + w * C::TM_GROUP + 2 * C::TM_S + b * 16 + lanes, o);
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ms->o_free[w][b]));
+            if (valid) {
+                __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out_o) + (slice * a.n + (long long)i * 16) * D + dd;
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    const float4 pz = *reinterpret_cast<const float4*>(ms->ecs[w][b][c]);
+                    float val = o[c] * ms->izs[w][b][c];
+                    val = fmaf(pz.x, vcp[0], val);
+                    val = fmaf(pz.y, vcp[1], val);
+                    val = fmaf(pz.z, vcp[2], val);
+                    val = fmaf(pz.w, vcp[3], val);
+                    dst[c * D] = __float2bfloat16_rn(val);
+                }
+            }
+        };
+
+        if (nblk > 0) {
+            coarse(0, 0);
+            named_barrier(1 + w, 128);
+        }
+        float vc_prev[4] = {0.f, 0.f, 0.f, 0.f};
+        int cb = 0;  // coarse buffer of block j: j % 3
+        for (long long j = 0; j < nblk; j++) {
+            const long long bl = w + 2 * j;
+            const int b = (int)(j & 1);
+            const uint32_t use = (uint32_t)(j >> 1);
+            const int st = (int)(bl % C::STAGES);
+            const long long g = blockIdx.x + bl * G;
+            const long long slice = g / a.T;
+            const int i = (int)(g - slice * a.T);
+            const float* sCk = reinterpret_cast<const float*>(stages + st * C::STAGE_BYTES + C::Q_BYTES + 2 * C::KV_BYTES);
+            const uint32_t tS = tbase + w * C::TM_GROUP + b * C::TM_S + lanes;
+            float m2[16];
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+                const float4 v = *reinterpret_cast<const float4*>(&ms->cmax[w][cb][c]);
+                m2[c] = v.x; m2[c + 1] = v.y; m2[c + 2] = v.z; m2[c + 3] = v.w;
+            }
+            mbar_wait(smem_u32(&ms->s_full[w][b]), use & 1, abort_flag, a.status);
+            tc_fence_after();
+            float s[NT][16];
+#pragma unroll
+            for (int t = 0; t < NT; t++) tmem_ld16(tS + t * 16, s[t]);
+            float x[16], amax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 16; c++) {
+                x[c] = 0.f;
+#pragma unroll
+                for (int t = 0; t < NT; t++) {
+                    const float arg = fmaf(s[t][c], scl2, -m2[c]);
+                    amax = fmaxf(amax, arg);
+                    s[t][c] = ex2(arg);
+                    x[c] += s[t][c];
+                }
+            }
+            // the next block's pooled logits, while this block's sums travel
+            const int cbn = cb == 2 ? 0 : cb + 1;
+            if (j + 1 < nblk) coarse(j + 1, cbn);
+            float r = warp_reduce16<false>(x, lane);
+            if (!(lane & 1)) ms->red_sum[w][b][lane >> 1][qr] = r;
+            const unsigned wide = __ballot_sync(0xffffffffu, !(amax <= kShiftSlack));
+            if (lane == 0) ms->flags[w][b][qr] = wide != 0u;
+            named_barrier(1 + w, 128);
+            const int4 fl = *reinterpret_cast<const int4*>(ms->flags[w][b]);
+            float fac[16];  // rescales the pooled sum to the final shift
+            if ((fl.x | fl.y | fl.z | fl.w) != 0) {
+                // exact row maxima from the raw S, still held in TMEM
+#pragma unroll
+                for (int t = 0; t < NT; t++) tmem_ld16(tS + t * 16, s[t]);
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    x[c] = s[0][c];
+#pragma unroll
+                    for (int t = 1; t < NT; t++) x[c] = fmaxf(x[c], s[t][c]);
+                }
+                r = warp_reduce16<true>(x, lane);
+                if (!(lane & 1)) ms->red_max[w][lane >> 1][qr] = r;
+                named_barrier(1 + w, 128);
+#pragma unroll
+                for (int c = 0; c < 16; c++) {
+                    const float4 rm = *reinterpret_cast<const float4*>(ms->red_max[w][c]);
+                    const float mn = fmaxf(m2[c], fmaxf(fmaxf(rm.x, rm.y), fmaxf(rm.z, rm.w)) * scl2);
+                    fac[c] = ex2(m2[c] - mn);
+                    m2[c] = mn;
+                    x[c] = 0.f;
+#pragma unroll
+                    for (int t = 0; t < NT; t++) {
+                        s[t][c] = ex2(fmaf(s[t][c], scl2, -m2[c]));
+                        x[c] += s[t][c];
+                    }
+                }
+                r = warp_reduce16<false>(x, lane);
+                if (!(lane & 1)) ms->red_sum[w][b][lane >> 1][qr] = r;
+                named_barrier(1 + w, 128);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 16; c++) fac[c] = 1.f;
+            }
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ms->s_free[w][b]));
+            // this thread's column of the pooled V rows, read while the stage is held
+            float vc[4];
+#pragma unroll
+            for (int l = 0; l < 4; l++) vc[l] = (l < Le && valid) ? sCk[(4 + l) * D + dd] : 0.f;
+            // unnormalised P (bf16, <= 2^kShiftSlack) as the [query][key]
+            // K-major operand; O is scaled by 1 / row sum in the epilogue
+            unsigned char* P = pbuf + (w * 2 + b) * C::P_BYTES;
+#pragma unroll
+            for (int t = 0; t < NT; t++) {
+                const int key = t * 128 + qr * 32 + lane;
+                unsigned char* pb = P + (key >> 6) * 2048 + (key & 7) * 2;
+                const int chk = (key & 63) >> 3;
+#pragma unroll
+                for (int c = 0; c < 16; c++)
+                    *reinterpret_cast<__nv_bfloat16*>(pb + c * 128 + ((chk ^ (c & 7)) << 4)) = __float2bfloat16_rn(s[t][c]);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ms->p_full[w][b]));
+            // while P V runs: row sums (fine keys + pooled keys), each >= 1
+            // because the shift is one of the logits or lies above all of them
+            if (tw < 64) {
+                const int q = tw >> 2, l = tw & 3;
+                float mq = 0.f, fq = 1.f;
+#pragma unroll
+                for (int c = 0; c < 16; c++)
+                    if (c == q) { mq = m2[c]; fq = fac[c]; }
+                const float4 rs = *reinterpret_cast<const float4*>(ms->red_sum[w][b][q]);
+                const float z = ((rs.x + rs.y) + (rs.z + rs.w)) + ms->csum[w][cb][q] * fq;
+                const float iz = rcp_approx(z);
+                ms->ecs[w][b][q][l] = ex2(ms->cs2[w][cb][q][l] - mq) * iz;
+                if (l == 0) {
+                    ms->izs[w][b][q] = iz;
+                    a.lse[slice * a.n + (long long)i * 16 + q] = mq * (1.0f / kLog2e) + logf(z);
+                }
+            }
+            if (j >= 1) epilogue(j - 1, vc_prev);
+#pragma unroll
+            for (int l = 0; l < 4; l++) vc_prev[l] = vc[l];
+            cb = cbn;
+        }
+        if (nblk > 0) epilogue(nblk - 1, vc_prev);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TM_ALLOC);
+    }
+}
+
+template <int D, int NT>
+int launch_pipe(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                const CUtensorMap& mv, cudaStream_t st) {
+    using C = PCfg<D, NT>;
+    static_assert(C::SMEM <= 227 * 1024 && C::STAGES >= 4, "shared memory budget");
+    static_assert(sizeof(PMisc) <= 8192, "misc block");
+    cudaFuncSetAttribute(fwd_tc_pipe_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const long long total = s.slices * (long long)s.T;
+    const int grid = (int)std::min<long long>(total, (long long)sm_count());
+    LLSA_LAUNCH("fwd_tc", st, fwd_tc_pipe_kernel<D, NT><<<grid, kThreads, C::SMEM, st>>>(mq, mk, mv, a));
+    return LLSA_OK;
+}
+
 template <int D, int NT>
 int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                const CUtensorMap& mv, cudaStream_t st) {
@@ -446,6 +949,14 @@ int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const C
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
     LLSA_LAUNCH("fwd_tc", st, fwd_tc_kernel<D, NT><<<grid, kThreads, C::SMEM, st>>>(mq, mk, mv, a));
     return LLSA_OK;
+}
+
+// the pipelined kernel where four stages fit, else the few-stage one
+template <int D, int NT>
+int launch_any(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
+               const CUtensorMap& mv, cudaStream_t st) {
+    if constexpr (pipe_fits<D, NT>()) return launch_pipe<D, NT>(s, a, mq, mk, mv, st);
+    else return launch_cfg<D, NT>(s, a, mq, mk, mv, st);
 }
 
 }  // namespace
@@ -461,8 +972,8 @@ int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     LLSA_TRY(make_tmap_bf16(&mq, a.q, rows, s.d, 16));
     LLSA_TRY(make_tmap_bf16(&mk, a.k, rows, s.d, 16));
     LLSA_TRY(make_tmap_bf16(&mv, a.v, rows, s.d, 16));
-    if (s.d == 64) return s.K1 == 8 ? launch_cfg<64, 1>(s, a, mq, mk, mv, st) : launch_cfg<64, 2>(s, a, mq, mk, mv, st);
-    return s.K1 == 8 ? launch_cfg<128, 1>(s, a, mq, mk, mv, st) : launch_cfg<128, 2>(s, a, mq, mk, mv, st);
+    if (s.d == 64) return s.K1 == 8 ? launch_any<64, 1>(s, a, mq, mk, mv, st) : launch_any<64, 2>(s, a, mq, mk, mv, st);
+    return s.K1 == 8 ? launch_any<128, 1>(s, a, mq, mk, mv, st) : launch_any<128, 2>(s, a, mq, mk, mv, st);
 }
 
 }  // namespace llsa

@@ -50,10 +50,6 @@ struct SelectArgs {
     int* status;
 };
 
-__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
-    return sa > sb || (sa == sb && ia < ib);
-}
-
 // Order-preserving map of a float to an unsigned key (for non-NaN inputs;
 // -0 and +0 map to the same key).
 __device__ __forceinline__ unsigned order_key(float v) {
