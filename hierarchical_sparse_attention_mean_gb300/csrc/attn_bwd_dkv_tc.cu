@@ -212,7 +212,15 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        // The whole warp runs the issue loop: lane 0 waits and broadcasts the
+        // result; MMAs and commits are issued by one lane elected inside the
+        // asm (a divergent branch around tcgen05.mma slows each issue).
+        {
+            auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(smem_u32(bar), parity, abort_flag, a.status) ? 1 : 0;
+                return __shfl_sync(0xffffffffu, ok, 0) != 0;
+            };
             constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
             constexpr uint32_t idG = idesc_bf16(D, 16, 1, 0);
             const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);         // K-major
@@ -227,31 +235,31 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             auto issue_S = [&](const Item& it) -> bool {
                 int st, u;
                 stage_of<C>(it.n, st, u);
-                if (!mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status)) return false;
-                if (it.k >= 1 && !mbar_wait(smem_u32(&ms->s_free[it.w]), (it.k - 1) & 1, abort_flag, a.status))
+                if (!wait1(&ms->full[st], u & 1)) return false;
+                if (it.k >= 1 && !wait1(&ms->s_free[it.w], (it.k - 1) & 1))
                     return false;
-                mbar_arrive(smem_u32(&ms->q_ready[it.w]));
+                if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w]));
                 tc_fence_after();
                 const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ks++) {
                     const uint32_t qoff = (ks / 4) * 128 * 128 + (ks % 4) * 32;
                     const uint32_t koff = (ks / 4) * 2048 + (ks % 4) * 32;
-                    mma_bf16(tbase + it.w * 32, dKm + ((s0 + qoff) >> 4), dKm + ((s0 + C::OFF_K + koff) >> 4), idS,
+                    mma_bf16_warp(tbase + it.w * 32, dKm + ((s0 + qoff) >> 4), dKm + ((s0 + C::OFF_K + koff) >> 4), idS,
                              ks > 0);
-                    mma_bf16(tbase + it.w * 32 + 16, dKm + ((s0 + C::OFF_DO + qoff) >> 4),
+                    mma_bf16_warp(tbase + it.w * 32 + 16, dKm + ((s0 + C::OFF_DO + qoff) >> 4),
                              dKm + ((s0 + C::OFF_V + koff) >> 4), idS, ks > 0);
                 }
-                mma_commit(smem_u32(&ms->s_full[it.w]));
+                mma_commit_warp(smem_u32(&ms->s_full[it.w]));
                 return true;
             };
             auto issue_G = [&](const Item& it) -> bool {
                 int st, u;
                 stage_of<C>(it.n, st, u);
-                if (!mbar_wait(smem_u32(&ms->p_full[it.w]), it.k & 1, abort_flag, a.status)) return false;
+                if (!wait1(&ms->p_full[it.w], it.k & 1)) return false;
                 // the accumulators are free once the previous key block's epilogue read them
                 if (it.gi == 0 && it.kn >= 1 &&
-                    !mbar_wait(smem_u32(&ms->acc_free[it.w]), (it.kn - 1) & 1, abort_flag, a.status))
+                    !wait1(&ms->acc_free[it.w], (it.kn - 1) & 1))
                     return false;
                 tc_fence_after();
                 const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
@@ -260,14 +268,14 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 for (int ks = 0; ks < 8; ks++) {
                     const uint32_t boff = pb + (ks / 4) * 2048 + (ks % 4) * 32;
                     const uint32_t acc = (it.gi > 0 || ks > 0) ? 1u : 0u;
-                    mma_bf16(tbase + 64 + it.w * 32 + 16, dMN + ((s0 + C::OFF_DO + ks * 2048) >> 4), dPB + (boff >> 4),
+                    mma_bf16_warp(tbase + 64 + it.w * 32 + 16, dMN + ((s0 + C::OFF_DO + ks * 2048) >> 4), dPB + (boff >> 4),
                              idG, acc);
-                    mma_bf16(tbase + 64 + it.w * 32, dMN + ((s0 + ks * 2048) >> 4), dPB + ((boff + C::PB_BYTES) >> 4),
+                    mma_bf16_warp(tbase + 64 + it.w * 32, dMN + ((s0 + ks * 2048) >> 4), dPB + ((boff + C::PB_BYTES) >> 4),
                              idG, acc);
                 }
-                mma_commit(smem_u32(&ms->p_free[it.w]));
-                mma_commit(smem_u32(&ms->empty[st]));
-                if (it.last) mma_commit(smem_u32(&ms->acc_full[it.w]));
+                mma_commit_warp(smem_u32(&ms->p_free[it.w]));
+                mma_commit_warp(smem_u32(&ms->empty[st]));
+                if (it.last) mma_commit_warp(smem_u32(&ms->acc_full[it.w]));
                 return true;
             };
             int kb = 0;
@@ -295,9 +303,10 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 have_pending = true;
             }
             if (ok && have_pending) issue_G(pending);
-            mma_commit(smem_u32(&ms->drain));
-            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
-            }
+            mma_commit_warp(smem_u32(&ms->drain));
+            if (lane == 0)
+                for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+                }
         }
         __syncwarp();
     } else if (warp >= 4) {
