@@ -16,9 +16,20 @@
 // the same K tile read as an MN-major operand (M = d, N = 16, K = keys). The
 // softmax needs no reduction here: lse is known.
 //
-// Warp roles as in the forward: up to three gather warps (TMA boxes for Q, dO,
-// o and the selected K and V blocks; bulk copies for pooled rows and lse),
-// one MMA thread, two warpgroups alternating query blocks.
+// Pooled keys: eight threads per query compute D_t and the query's dot
+// products with the pooled K and V rows (one 16-byte chunk of each row per 64
+// columns), so P, dS and D_t of a query are known without a group barrier.
+// The pooled-level partial gradients are two more MMAs per block:
+// gK^T = Q^T dS_c and gV^T = dO^T P_c (M = d, N = 16 with L_e <= 4 columns
+// used, K = the 16 queries), with dS_c and P_c stored as bf16 operands like
+// the fine-key dS.
+//
+// Warp roles: three gather warps split every block's copies (warp 0 the Q, dO
+// and o boxes, lse and the pooled rows; warp 2 the K blocks; warp 3 the V
+// blocks) into a ring of stages; warp 1 issues the MMAs out of order between
+// the S stream and the gradient stream (gradient first, as it frees a stage),
+// through an election inside the MMA asm; two warpgroups alternate query
+// blocks.
 #include <algorithm>
 
 #include "attn.h"
@@ -37,7 +48,6 @@ template <int D, int NT>
 struct Cfg {
     static constexpr int NF = NT * 128;
     static constexpr int REG = D / 64;
-    static constexpr int CH = D / 8;
     static constexpr int Q_BYTES = 16 * D * 2;
     static constexpr int KV_BYTES = NF * D * 2;
     static constexpr int CO_BYTES = 2 * 4 * D * 4;  // pooled K and V rows (fp32)
@@ -46,34 +56,21 @@ struct Cfg {
     static constexpr int OFF_V = OFF_K + KV_BYTES, OFF_C = OFF_V + KV_BYTES, OFF_L = OFF_C + CO_BYTES;
     static constexpr int STAGE_BYTES = OFF_L + 1024;
     static constexpr int DS_BYTES = 16 * NF * 2;  // per warpgroup
-    static constexpr int FIXED = 2 * DS_BYTES + 4096;
+    static constexpr int BC_BYTES = 2048;         // per warpgroup and operand: 16 rows x 128 B
+    static constexpr int FIXED = 2 * DS_BYTES + 4 * BC_BYTES + 4096;
     static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
-    static constexpr int NPROD = STAGES_RAW >= 3 ? 3 : (STAGES_RAW >= 2 ? 2 : 1);
-    static constexpr int SPP = (STAGES_RAW < 1 ? 1 : (STAGES_RAW > 6 ? 6 : STAGES_RAW)) / NPROD;
-    static constexpr int STAGES = NPROD * SPP;
+    static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
-    static constexpr int TM_GROUP = 128;  // per warpgroup: S at +0, dP at +32, dq at +64
+    static constexpr int TM_GROUP = 128;  // per warpgroup: S +0, dP +32, dq +64, gK +96, gV +112
 };
-
-template <class C>
-__device__ __forceinline__ void stage_of(int bl, int& st, int& u) {
-    const int k = bl / C::NPROD;
-    st = (bl % C::NPROD) * C::SPP + k % C::SPP;
-    u = k / C::SPP;
-}
 
 struct Misc {
     float dsum[2][16];       // D_t
-    float cp[2][16][4];      // pooled-key P
-    float cds[2][16][4];     // pooled-key dS
-    uint64_t full[6], empty[6], q_ready[2], s_full[2], ds_full[2], dq_full[2], s_free[2], o_free[2], drain;
+    float cds[2][2][16][4];  // pooled-key dS, [group][block parity][query][level]
+    uint64_t full[6], empty[6], q_ready[2], s_full[2], ds_full[2], g_full[2], s_free[2], o_free[2], drain;
     uint32_t tmem_slot;
     int abort_flag;
 };
-
-__device__ __forceinline__ float bf16_at(const unsigned char* tile, int row, int col) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(tile + sw128_offset(row, col, 16)));
-}
 
 template <int D, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -87,24 +84,26 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stages = sm;
     unsigned char* dsbuf = stages + C::STAGES * C::STAGE_BYTES;
-    Misc* ms = reinterpret_cast<Misc*>(dsbuf + 2 * C::DS_BYTES);
+    unsigned char* bcbuf = dsbuf + 2 * C::DS_BYTES;  // [group][dS_c, P_c]
+    Misc* ms = reinterpret_cast<Misc*>(bcbuf + 4 * C::BC_BYTES);
     volatile int* abort_flag = &ms->abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long total = a.slices * (long long)a.T;
     const int G = gridDim.x;
     const int K1 = NT * 8, Le = a.Le;
+    const long long mine = total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
-            mbar_init(smem_u32(&ms->full[s]), 1);
+            mbar_init(smem_u32(&ms->full[s]), 3);  // one arrival per gather warp
             mbar_init(smem_u32(&ms->empty[s]), 1);
         }
         for (int w = 0; w < 2; w++) {
             mbar_init(smem_u32(&ms->q_ready[w]), 1);
             mbar_init(smem_u32(&ms->s_full[w]), 1);
             mbar_init(smem_u32(&ms->ds_full[w]), 128);
-            mbar_init(smem_u32(&ms->dq_full[w]), 1);
+            mbar_init(smem_u32(&ms->g_full[w]), 1);
             mbar_init(smem_u32(&ms->s_free[w]), 128);
             mbar_init(smem_u32(&ms->o_free[w]), 128);
         }
@@ -112,156 +111,181 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         ms->abort_flag = 0;
         fence_mbar_init();
     }
-    for (int x = threadIdx.x; x < 2 * 16 * 4; x += kThreads) {
-        (&ms->cp[0][0][0])[x] = 0.f;
-        (&ms->cds[0][0][0])[x] = 0.f;
-    }
+    // rows L_e..15 of the pooled operands stay zero
+    for (int x = threadIdx.x; x < 4 * C::BC_BYTES / 16; x += kThreads)
+        reinterpret_cast<uint4*>(bcbuf)[x] = make_uint4(0u, 0u, 0u, 0u);
+    fence_async_smem();
     if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tbase = ms->tmem_slot;
 
-    if ((warp == 0 || warp == 2 || warp == 3) && (warp == 0 ? 0 : warp - 1) < C::NPROD) {
+    if (warp == 0 || warp == 2 || warp == 3) {
         // ----------------------------------------------------------- gather
-        const int pw = warp == 0 ? 0 : warp - 1;
-        auto load_idx = [&](int bl, int& jb, int& ce) {
-            const long long g = blockIdx.x + (long long)bl * G;
-            jb = 0;
-            ce = 0;
-            if (g >= total) return;
+        // Block bl uses stage bl % STAGES for the (bl / STAGES)-th time; each
+        // warp arrives on the stage barrier with the bytes of its own copies.
+        const int role = warp == 0 ? 0 : warp - 1;
+        auto load_idx = [&](long long bl) -> int {
+            if (bl >= mine) return 0;
+            const long long g = blockIdx.x + bl * G;
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
-            if (lane < K1) jb = a.sel[(slice * a.T + i) * a.K1 + lane];
-            if (lane < Le) ce = a.coarse[(slice * a.T + i) * a.L + lane];
+            if (role == 0) return lane < Le ? a.coarse[(slice * a.T + i) * a.L + lane] : 0;
+            return lane < K1 ? a.sel[(slice * a.T + i) * a.K1 + lane] : 0;
         };
-        int jb0, ce0, jb1, ce1;
-        load_idx(pw, jb0, ce0);
-        load_idx(pw + C::NPROD, jb1, ce1);
-        int issued = -1;
-        for (int bl = pw;; bl += C::NPROD) {
-            const long long g = blockIdx.x + (long long)bl * G;
-            if (g >= total) break;
-            int jb = jb0, e = ce0;
-            jb0 = jb1;
-            ce0 = ce1;
-            load_idx(bl + 2 * C::NPROD, jb1, ce1);
-            int st, u;
-            stage_of<C>(bl, st, u);
+        const uint32_t my_bytes = role == 0 ? 3 * C::Q_BYTES + 64 + 2 * Le * D * 4 : C::KV_BYTES;
+        int ix0 = load_idx(0), ix1 = load_idx(1);
+        long long issued = -1;
+        for (long long bl = 0; bl < mine; bl++) {
+            int ix = ix0;
+            ix0 = ix1;
+            ix1 = load_idx(bl + 2);
+            const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
             bool ok = true;
             if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
+            const long long g = blockIdx.x + bl * G;
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
             unsigned char* sb = stages + st * C::STAGE_BYTES;
             const uint32_t fb = smem_u32(&ms->full[st]);
-            if (lane == 0) mbar_arrive_expect_tx(fb, 3 * C::Q_BYTES + 2 * C::KV_BYTES + 2 * Le * D * 4 + 64);
+            if (lane == 0) mbar_arrive_expect_tx(fb, my_bytes);
             __syncwarp();
             const long long tok0 = slice * a.n + (long long)i * 16;
-            if (lane == 0) {
-                for (int r = 0; r < C::REG; r++) {
-                    tma_load_2d(smem_u32(sb + r * 2048), &mq, r * 64, (int)tok0, fb);
-                    tma_load_2d(smem_u32(sb + C::OFF_DO + r * 2048), &mdo, r * 64, (int)tok0, fb);
-                    tma_load_2d(smem_u32(sb + C::OFF_O + r * 2048), &mo, r * 64, (int)tok0, fb);
+            if (role == 0) {
+                if (lane == 0) {
+                    for (int r = 0; r < C::REG; r++) {
+                        tma_load_2d(smem_u32(sb + r * 2048), &mq, r * 64, (int)tok0, fb);
+                        tma_load_2d(smem_u32(sb + C::OFF_DO + r * 2048), &mdo, r * 64, (int)tok0, fb);
+                        tma_load_2d(smem_u32(sb + C::OFF_O + r * 2048), &mo, r * 64, (int)tok0, fb);
+                    }
+                    bulk_load(smem_u32(sb + C::OFF_L), a.lse_in + tok0, 64, fb);
                 }
-                bulk_load(smem_u32(sb + C::OFF_L), a.lse_in + tok0, 64, fb);
-            }
-            if (lane < K1) {
-                if (jb < 0 || jb >= a.T) {
+                if (lane < Le) {
+                    if (ix < 0 || ix >= a.lv.n_level[lane + 1]) {
+                        set_status(a.status, LLSA_ERR_BAD_INDEX);
+                        ix = 0;
+                    }
+                    const long long row = slice * a.pyr_stride + (long long)(a.lv.row_offset[lane + 1] + ix) * D;
+                    bulk_load(smem_u32(sb + C::OFF_C + lane * D * 4), a.kpyr + row, D * 4, fb);
+                    bulk_load(smem_u32(sb + C::OFF_C + (4 + lane) * D * 4), a.vpyr + row, D * 4, fb);
+                }
+            } else if (lane < K1) {
+                if (ix < 0 || ix >= a.T) {
                     set_status(a.status, LLSA_ERR_BAD_INDEX);
-                    jb = 0;
+                    ix = 0;
                 }
-                const int yk = (int)(slice * a.n + (long long)jb * 16);
+                const int yk = (int)(slice * a.n + (long long)ix * 16);
                 for (int r = 0; r < C::REG; r++) {
-                    tma_load_2d(smem_u32(sb + C::OFF_K + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
-                    tma_load_2d(smem_u32(sb + C::OFF_V + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    if (role == 1) tma_load_2d(smem_u32(sb + C::OFF_K + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
+                    else tma_load_2d(smem_u32(sb + C::OFF_V + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
                 }
-            }
-            if (lane < Le) {
-                if (e < 0 || e >= a.lv.n_level[lane + 1]) {
-                    set_status(a.status, LLSA_ERR_BAD_INDEX);
-                    e = 0;
-                }
-                const long long row = slice * a.pyr_stride + (long long)(a.lv.row_offset[lane + 1] + e) * D;
-                bulk_load(smem_u32(sb + C::OFF_C + lane * D * 4), a.kpyr + row, D * 4, fb);
-                bulk_load(smem_u32(sb + C::OFF_C + (4 + lane) * D * 4), a.vpyr + row, D * 4, fb);
             }
             issued = bl;
         }
+        // copies still in flight must land before the CTA exits
         if (lane == 0)
-            for (int bl = issued; bl >= 0 && bl > issued - C::NPROD * C::SPP; bl -= C::NPROD) {
-                int st, u;
-                stage_of<C>(bl, st, u);
+            for (long long bl = issued; bl >= 0 && bl > issued - C::STAGES; bl--) {
+                const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
                 for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->full[st]), u & 1); it++) {
                 }
             }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
-            constexpr uint32_t idQ = idesc_bf16(D, 16, 1, 0);
-            const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);            // K-major
-            const uint64_t dMN = desc_sw128(smem_u32(stages), C::NF * 128, 1024);   // K tile as MN-major
-            const uint64_t dDS = desc_sw128(smem_u32(dsbuf), 16, 1024);
-            auto issue_S = [&](int bl) -> bool {
-                const int w = bl & 1, j = bl >> 1;
-                int st, u;
-                stage_of<C>(bl, st, u);
-                if (!mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status)) return false;
-                mbar_arrive(smem_u32(&ms->q_ready[w]));
-                if (j >= 1 && !mbar_wait(smem_u32(&ms->s_free[w]), (j - 1) & 1, abort_flag, a.status)) return false;
-                tc_fence_after();
-                const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
+        constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
+        constexpr uint32_t idQ = idesc_bf16(D, 16, 1, 0);
+        const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);            // K-major
+        const uint64_t dMN = desc_sw128(smem_u32(stages), C::NF * 128, 1024);   // K tile as MN-major
+        const uint64_t dQT = desc_sw128(smem_u32(stages), 16 * 128, 1024);      // Q / dO tiles as MN-major
+        const uint64_t dDS = desc_sw128(smem_u32(dsbuf), 16, 1024);
+        const uint64_t dBC = desc_sw128(smem_u32(bcbuf), 16, 1024);
+        // block bl: group bl & 1, its j-th block
+        auto s_ready = [&](long long bl) -> bool {
+            const int w = (int)(bl & 1);
+            const uint32_t j = (uint32_t)(bl >> 1);
+            const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
+            return mbar_test(smem_u32(&ms->full[st]), u & 1) &&
+                   (j == 0 || mbar_test(smem_u32(&ms->s_free[w]), (j - 1) & 1));
+        };
+        auto g_ready = [&](long long bl) -> bool {
+            const int w = (int)(bl & 1);
+            const uint32_t j = (uint32_t)(bl >> 1);
+            return mbar_test(smem_u32(&ms->ds_full[w]), j & 1) &&
+                   (j == 0 || mbar_test(smem_u32(&ms->o_free[w]), (j - 1) & 1));
+        };
+        auto issue_S = [&](long long bl) {
+            const int w = (int)(bl & 1);
+            const int st = (int)(bl % C::STAGES);
+            if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[w]));  // the group may read the stage
+            tc_fence_after();
+            const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
 #pragma unroll
-                for (int t = 0; t < NT; t++)
+            for (int t = 0; t < NT; t++)
 #pragma unroll
-                    for (int ks = 0; ks < D / 16; ks++) {
-                        const uint32_t koff = (ks / 4) * C::NF * 128 + t * 128 * 128 + (ks % 4) * 32;
-                        const uint32_t qoff = (ks / 4) * 2048 + (ks % 4) * 32;
-                        mma_bf16(tbase + w * C::TM_GROUP + t * 16, dKm + ((s0 + C::OFF_K + koff) >> 4),
-                                 dKm + ((s0 + qoff) >> 4), idS, ks > 0);
-                        mma_bf16(tbase + w * C::TM_GROUP + 32 + t * 16, dKm + ((s0 + C::OFF_V + koff) >> 4),
-                                 dKm + ((s0 + C::OFF_DO + qoff) >> 4), idS, ks > 0);
-                    }
-                mma_commit(smem_u32(&ms->s_full[w]));
-                return true;
-            };
-            auto issue_DQ = [&](int bl) -> bool {
-                const int w = bl & 1, j = bl >> 1;
-                int st, u;
-                stage_of<C>(bl, st, u);
-                if (!mbar_wait(smem_u32(&ms->ds_full[w]), j & 1, abort_flag, a.status)) return false;
-                if (j >= 1 && !mbar_wait(smem_u32(&ms->o_free[w]), (j - 1) & 1, abort_flag, a.status)) return false;
-                tc_fence_after();
-                const uint32_t k0 = (uint32_t)(st * C::STAGE_BYTES + C::OFF_K);
-                const uint32_t d0 = (uint32_t)(w * C::DS_BYTES);
-#pragma unroll
-                for (int ks = 0; ks < C::NF / 16; ks++)
-                    mma_bf16(tbase + w * C::TM_GROUP + 64, dMN + ((k0 + ks * 2048) >> 4),
-                             dDS + ((d0 + (ks / 4) * 2048 + (ks % 4) * 32) >> 4), idQ, ks > 0);
-                mma_commit(smem_u32(&ms->dq_full[w]));
-                mma_commit(smem_u32(&ms->empty[st]));
-                return true;
-            };
-            const long long mine = total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
-            bool ok = true;
-            if (C::STAGES >= 2) {
-                ok = mine > 0 ? issue_S(0) : true;
-                for (long long bl = 0; ok && bl < mine; bl++) {
-                    if (bl + 1 < mine) ok = issue_S((int)bl + 1);
-                    if (ok) ok = issue_DQ((int)bl);
+                for (int ks = 0; ks < D / 16; ks++) {
+                    const uint32_t koff = (ks / 4) * C::NF * 128 + t * 128 * 128 + (ks % 4) * 32;
+                    const uint32_t qoff = (ks / 4) * 2048 + (ks % 4) * 32;
+                    mma_bf16_warp(tbase + w * C::TM_GROUP + t * 16, dKm + ((s0 + C::OFF_K + koff) >> 4),
+                                  dKm + ((s0 + qoff) >> 4), idS, ks > 0);
+                    mma_bf16_warp(tbase + w * C::TM_GROUP + 32 + t * 16, dKm + ((s0 + C::OFF_V + koff) >> 4),
+                                  dKm + ((s0 + C::OFF_DO + qoff) >> 4), idS, ks > 0);
                 }
-            } else {
-                for (long long bl = 0; ok && bl < mine; bl++) {
-                    ok = issue_S((int)bl);
-                    if (ok) ok = issue_DQ((int)bl);
-                }
+            mma_commit_warp(smem_u32(&ms->s_full[w]));
+        };
+        auto issue_G = [&](long long bl) {
+            const int w = (int)(bl & 1);
+            const int st = (int)(bl % C::STAGES);
+            tc_fence_after();
+            const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
+            const uint32_t d0 = (uint32_t)(w * C::DS_BYTES);
+            const uint32_t b0 = (uint32_t)(w * 2 * C::BC_BYTES);
+            const uint32_t tg = tbase + w * C::TM_GROUP;
+#pragma unroll
+            for (int ks = 0; ks < C::NF / 16; ks++)
+                mma_bf16_warp(tg + 64, dMN + ((s0 + C::OFF_K + ks * 2048) >> 4),
+                              dDS + ((d0 + (ks / 4) * 2048 + (ks % 4) * 32) >> 4), idQ, ks > 0);
+            mma_bf16_warp(tg + 96, dQT + (s0 >> 4), dBC + (b0 >> 4), idQ, 0);
+            mma_bf16_warp(tg + 112, dQT + ((s0 + C::OFF_DO) >> 4), dBC + ((b0 + C::BC_BYTES) >> 4), idQ, 0);
+            mma_commit_warp(smem_u32(&ms->g_full[w]));
+            mma_commit_warp(smem_u32(&ms->empty[st]));
+        };
+        // out of order between the two in-order streams; idle polls bounded
+        long long nS = 0, nG = 0;
+        int idle = 0;
+        while (nG < mine) {
+            int act = 0;
+            if (lane == 0) {
+                if (nG < nS && g_ready(nG)) act = 2;
+                else if (nS < mine && s_ready(nS)) act = 1;
             }
-            mma_commit(smem_u32(&ms->drain));
-            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+            act = __shfl_sync(0xffffffffu, act, 0);
+            if (act == 1) {
+                issue_S(nS++);
+                idle = 0;
+            } else if (act == 2) {
+                issue_G(nG++);
+                idle = 0;
+            } else {
+                int stop = 0;
+                if (lane == 0) {
+                    if (++idle >= kSpinLimit) {
+                        *abort_flag = 1;
+                        set_status(a.status, LLSA_ERR_TIMEOUT);
+                        stop = 1;
+                    } else if ((idle & 63) == 0 && *abort_flag) {
+                        stop = 1;
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
             }
         }
+        // no MMA may be in flight when TMEM is released
+        mma_commit_warp(smem_u32(&ms->drain));
+        if (lane == 0)
+            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+            }
         __syncwarp();
     } else if (warp >= 4) {
         // --------------------------------------------- elementwise + epilogue
@@ -271,16 +295,13 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const float sc = a.scale, scl2 = a.scale * kLog2e;
         const int dd = D == 64 ? 16 * qr + lane : 32 * qr + lane;
         const bool valid = D == 64 ? lane < 16 : true;
-        const int pi = tw >> 1, half = tw & 1;
-        const bool pact = pi < 16 * Le;
-        const int pq = pact ? pi / Le : 0, pl = pact ? pi % Le : 0;
+        const int cq = tw >> 3, cpart = tw & 7;  // pooled role: query, chunk
         unsigned char* DS = dsbuf + w * C::DS_BYTES;
-        for (int bl = w;; bl += 2) {
-            const long long g = blockIdx.x + (long long)bl * G;
-            if (g >= total) break;
-            const int j = bl >> 1;
-            int st, u;
-            stage_of<C>(bl, st, u);
+        unsigned char* BCs = bcbuf + w * 2 * C::BC_BYTES;  // dS_c; P_c follows
+        for (long long bl = w; bl < mine; bl += 2) {
+            const long long g = blockIdx.x + bl * G;
+            const uint32_t j = (uint32_t)(bl >> 1);
+            const int st = (int)(bl % C::STAGES);
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
             const long long tok0 = slice * a.n + (long long)i * 16;
@@ -290,30 +311,77 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             // waits return at once after a timeout; the group keeps walking the
             // same barriers so that no thread waits on another
             mbar_wait(smem_u32(&ms->q_ready[w]), j & 1, abort_flag, a.status);
-            // D_t = dO_t . o_t: eight threads per row, D/64 chunks of 8 each
+            // D_t = dO_t . o_t and the pooled-key dots q_t . k_l, dO_t . v_l:
+            // eight threads per query, one 16-byte chunk per 64 columns each
             {
-                const int row = tw >> 3, part = tw & 7;
-                float acc = 0.f;
+                float dsa = 0.f, sa[4] = {0.f, 0.f, 0.f, 0.f}, pa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int c8 = part; c8 < C::CH; c8 += 8) {
-                    const uint4 g4 = *reinterpret_cast<const uint4*>(sb + C::OFF_DO + sw128_offset(row, c8 * 8, 16));
-                    const uint4 o4 = *reinterpret_cast<const uint4*>(sb + C::OFF_O + sw128_offset(row, c8 * 8, 16));
+                for (int cc = 0; cc < D / 64; cc++) {
+                    const int c8 = cpart + 8 * cc;
+                    const uint32_t off = sw128_offset(cq, c8 * 8, 16);
+                    const uint4 q4 = *reinterpret_cast<const uint4*>(sb + off);
+                    const uint4 g4 = *reinterpret_cast<const uint4*>(sb + C::OFF_DO + off);
+                    const uint4 o4 = *reinterpret_cast<const uint4*>(sb + C::OFF_O + off);
+                    const __nv_bfloat162* qh = reinterpret_cast<const __nv_bfloat162*>(&q4);
                     const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&g4);
                     const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&o4);
+                    float qf[8], gf[8];
 #pragma unroll
                     for (int h = 0; h < 4; h++) {
-                        const float2 gf = __bfloat1622float2(gh[h]), of = __bfloat1622float2(oh[h]);
-                        acc = fmaf(gf.x, of.x, acc);
-                        acc = fmaf(gf.y, of.y, acc);
+                        const float2 qv = __bfloat1622float2(qh[h]), gv = __bfloat1622float2(gh[h]);
+                        const float2 ov = __bfloat1622float2(oh[h]);
+                        qf[2 * h] = qv.x; qf[2 * h + 1] = qv.y;
+                        gf[2 * h] = gv.x; gf[2 * h + 1] = gv.y;
+                        dsa = fmaf(gv.x, ov.x, dsa);
+                        dsa = fmaf(gv.y, ov.y, dsa);
+                    }
+#pragma unroll
+                    for (int l = 0; l < 4; l++)
+                        if (l < Le) {
+                            const float4 k0 = *reinterpret_cast<const float4*>(sKc + l * D + c8 * 8);
+                            const float4 k1 = *reinterpret_cast<const float4*>(sKc + l * D + c8 * 8 + 4);
+                            const float4 v0 = *reinterpret_cast<const float4*>(sKc + (4 + l) * D + c8 * 8);
+                            const float4 v1 = *reinterpret_cast<const float4*>(sKc + (4 + l) * D + c8 * 8 + 4);
+                            sa[l] = fmaf(qf[0], k0.x, sa[l]); sa[l] = fmaf(qf[1], k0.y, sa[l]);
+                            sa[l] = fmaf(qf[2], k0.z, sa[l]); sa[l] = fmaf(qf[3], k0.w, sa[l]);
+                            sa[l] = fmaf(qf[4], k1.x, sa[l]); sa[l] = fmaf(qf[5], k1.y, sa[l]);
+                            sa[l] = fmaf(qf[6], k1.z, sa[l]); sa[l] = fmaf(qf[7], k1.w, sa[l]);
+                            pa[l] = fmaf(gf[0], v0.x, pa[l]); pa[l] = fmaf(gf[1], v0.y, pa[l]);
+                            pa[l] = fmaf(gf[2], v0.z, pa[l]); pa[l] = fmaf(gf[3], v0.w, pa[l]);
+                            pa[l] = fmaf(gf[4], v1.x, pa[l]); pa[l] = fmaf(gf[5], v1.y, pa[l]);
+                            pa[l] = fmaf(gf[6], v1.z, pa[l]); pa[l] = fmaf(gf[7], v1.w, pa[l]);
+                        }
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    dsa += __shfl_xor_sync(0xffffffffu, dsa, o);
+#pragma unroll
+                    for (int l = 0; l < 4; l++) {
+                        sa[l] += __shfl_xor_sync(0xffffffffu, sa[l], o);
+                        pa[l] += __shfl_xor_sync(0xffffffffu, pa[l], o);
                     }
                 }
-                acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-                acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-                if (part == 0) {
-                    ms->dsum[w][row] = acc;
+                const float lq = sLse[cq];
+                float pc = 0.f, dsc = 0.f;  // this thread's level: cpart (< 4)
+#pragma unroll
+                for (int l = 0; l < 4; l++) {
+                    const float s = sc * sa[l] + (float)(l + 1) * a.lnB;
+                    const float p = l < Le ? ex2((s - lq) * kLog2e) : 0.f;
+                    if (l == cpart) {
+                        pc = p;
+                        dsc = p * (pa[l] - dsa);
+                    }
+                }
+                if (cpart == 0) {
+                    ms->dsum[w][cq] = dsa;
                     // (lse, D) pairs: the key-major kernel fetches both with one copy
-                    *reinterpret_cast<float2*>(a.Dbuf + 2 * (tok0 + row)) = make_float2(sLse[row], acc);
+                    *reinterpret_cast<float2*>(a.Dbuf + 2 * (tok0 + cq)) = make_float2(lq, dsa);
+                }
+                if (cpart < 4) {
+                    ms->cds[w][j & 1][cq][cpart] = dsc;
+                    const uint32_t bo = sw128_offset(cpart, cq, 16);
+                    *reinterpret_cast<__nv_bfloat16*>(BCs + bo) = __float2bfloat16_rn(dsc);
+                    *reinterpret_cast<__nv_bfloat16*>(BCs + C::BC_BYTES + bo) = __float2bfloat16_rn(pc);
                 }
             }
             // this thread's column of the pooled K rows (for dq's pooled term)
@@ -321,53 +389,6 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
 #pragma unroll
             for (int l = 0; l < 4; l++) kc[l] = (l < Le && valid) ? sKc[l * D + dd] : 0.f;
             named_barrier(1 + w, 128);
-            // pooled keys: two threads per (query, level)
-            {
-                float s0 = 0.f, s1 = 0.f, p0 = 0.f, p1 = 0.f;
-                if (pact) {
-                    const float* kr = sKc + pl * D;
-                    const float* vr = sKc + (4 + pl) * D;
-#pragma unroll
-                    for (int c8 = half * C::CH / 2; c8 < (half + 1) * C::CH / 2; c8++) {
-                        const uint4 q4 = *reinterpret_cast<const uint4*>(sb + sw128_offset(pq, c8 * 8, 16));
-                        const uint4 g4 = *reinterpret_cast<const uint4*>(sb + C::OFF_DO + sw128_offset(pq, c8 * 8, 16));
-                        const __nv_bfloat162* qh = reinterpret_cast<const __nv_bfloat162*>(&q4);
-                        const __nv_bfloat162* gh = reinterpret_cast<const __nv_bfloat162*>(&g4);
-#pragma unroll
-                        for (int h = 0; h < 4; h++) {
-                            const float2 qf = __bfloat1622float2(qh[h]), gf = __bfloat1622float2(gh[h]);
-                            const float2 kf = *reinterpret_cast<const float2*>(kr + c8 * 8 + 2 * h);
-                            const float2 vf = *reinterpret_cast<const float2*>(vr + c8 * 8 + 2 * h);
-                            s0 = fmaf(qf.x, kf.x, s0); s1 = fmaf(qf.y, kf.y, s1);
-                            p0 = fmaf(gf.x, vf.x, p0); p1 = fmaf(gf.y, vf.y, p1);
-                        }
-                    }
-                }
-                float sdot = s0 + s1, pdot = p0 + p1;
-                sdot += __shfl_xor_sync(0xffffffffu, sdot, 1);
-                pdot += __shfl_xor_sync(0xffffffffu, pdot, 1);
-                if (pact && half == 0) {
-                    const float s = sc * sdot + (float)(pl + 1) * a.lnB;
-                    const float p = ex2((s - sLse[pq]) * kLog2e);
-                    ms->cp[w][pq][pl] = p;
-                    ms->cds[w][pq][pl] = p * (pdot - ms->dsum[w][pq]);
-                }
-            }
-            named_barrier(1 + w, 128);
-            // partial gradients of the pooled keys and values of this block:
-            // gK = scale * sum_t dS_t q_t, gV = sum_t P_t dO_t
-            for (int it = tw; it < Le * D; it += 128) {
-                const int l = it / D, c = it % D;
-                float gk = 0.f, gv = 0.f;
-#pragma unroll
-                for (int t = 0; t < 16; t++) {
-                    gk = fmaf(ms->cds[w][t][l], bf16_at(sb, t, c), gk);
-                    gv = fmaf(ms->cp[w][t][l], bf16_at(sb + C::OFF_DO, t, c), gv);
-                }
-                const long long off = ((slice * a.T + i) * a.Le + l) * (long long)D + c;
-                a.gK[off] = sc * gk;
-                a.gV[off] = gv;
-            }
             // dS^T for the fine keys from S^T and dP^T
             float lse2[16], dsm[16];
 #pragma unroll
@@ -398,18 +419,21 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             mbar_arrive(smem_u32(&ms->s_free[w]));
             fence_async_smem();
             mbar_arrive(smem_u32(&ms->ds_full[w]));
-            // epilogue: dq^T from TMEM plus the pooled keys' term, times scale
-            mbar_wait(smem_u32(&ms->dq_full[w]), j & 1, abort_flag, a.status);
+            // epilogue: dq^T plus the pooled keys' term, times scale; the
+            // pooled-level partial gradients of this block
+            mbar_wait(smem_u32(&ms->g_full[w]), j & 1, abort_flag, a.status);
             tc_fence_after();
-            float q[16];
+            float q[16], gk[16], gv[16];
             tmem_ld16(tS + 64, q);
+            tmem_ld16(tS + 96, gk);
+            tmem_ld16(tS + 112, gv);
             tc_fence_before();
             mbar_arrive(smem_u32(&ms->o_free[w]));
             if (valid) {
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + tok0 * D + dd;
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
-                    const float4 g4 = *reinterpret_cast<const float4*>(ms->cds[w][c]);
+                    const float4 g4 = *reinterpret_cast<const float4*>(ms->cds[w][j & 1][c]);
                     float val = q[c];
                     val = fmaf(g4.x, kc[0], val);
                     val = fmaf(g4.y, kc[1], val);
@@ -417,6 +441,13 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                     val = fmaf(g4.w, kc[3], val);
                     dst[c * D] = __float2bfloat16_rn(sc * val);
                 }
+                const long long off = (slice * a.T + i) * (long long)a.Le * D + dd;
+#pragma unroll
+                for (int l = 0; l < 4; l++)
+                    if (l < Le) {
+                        a.gK[off + (long long)l * D] = sc * gk[l];
+                        a.gV[off + (long long)l * D] = gv[l];
+                    }
             }
         }
     }
@@ -433,6 +464,7 @@ int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaS
     using C = Cfg<D, NT>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(Misc) <= 4096, "misc block");
+    static_assert(C::STAGES >= 1, "one stage at least");
     cudaFuncSetAttribute(bwd_dq_tc_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
