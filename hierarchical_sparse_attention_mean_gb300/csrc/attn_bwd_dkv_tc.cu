@@ -12,11 +12,19 @@
 //
 // The column's query blocks are stacked eight at a time (M = 128 query rows):
 // S = Q_stack K_j^T and dP = dO_stack V_j^T (N = 16 keys), one TMEM lane per
-// query row, so P and dS need only that row's lse and D; then
-// dv^T += dO_stack^T P and dk^T += Q_stack^T dS (M = d, N = 16, K = 128 rows)
-// accumulate in TMEM across the column's groups, in CSC order (deterministic).
-// Each (key block, group of eight) is one item; items follow the key blocks of
-// the CTA in order; the two warpgroups take alternate key blocks.
+// query row, so P and dS need only that row's lse and D; then the gradients
+// accumulate in TMEM across the column's groups, in CSC order (deterministic):
+// for d = 64 one MMA per 16 rows computes [Q_stack ; dO_stack]^T [dS | P]
+// (M = 128, N = 32) whose diagonal blocks are dk^T and dv^T; for d = 128,
+// dk^T += Q_stack^T dS and dv^T += dO_stack^T P (M = d, N = 16). Each (key
+// block, group of eight) is one item; items follow the key blocks of the CTA
+// in order; the two warpgroups take alternate key blocks.
+//
+// Warp roles: three gather warps split every item's copies (warp 0 K_j, V_j
+// and the (lse, D) rows; warp 2 the Q stack; warp 3 the dO stack) into a ring
+// of stages; warp 1 issues the MMAs out of order between the S stream and the
+// gradient stream (gradient first, as it frees a stage), through an election
+// inside the MMA asm.
 #include <algorithm>
 
 #include "attn.h"
@@ -28,7 +36,7 @@ namespace {
 using namespace tc;
 
 constexpr int kThreads = 384;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kSmemBudget = 215 * 1024;
 constexpr int kMaxKeyBlocks = 2048;  // key blocks per CTA (counts kept in shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -41,21 +49,15 @@ struct Cfg {
     static constexpr int OFF_DO = QS_BYTES, OFF_K = 2 * QS_BYTES, OFF_V = OFF_K + KB_BYTES;
     static constexpr int OFF_LD = OFF_V + KB_BYTES;
     static constexpr int STAGE_BYTES = OFF_LD + 1024;
-    static constexpr int PB_BYTES = 16 * 128 * 2;  // P^T or dS^T of one item
-    static constexpr int FIXED = 4 * PB_BYTES + 4096 + kMaxKeyBlocks * 12;
+    // per warpgroup: dS^T and P^T of one item as K-major operands, interleaved
+    // per 64 rows (dS^T chunk c at c * 4096, P^T chunk c at c * 4096 + 2048)
+    static constexpr int PG_BYTES = 8192;
+    static constexpr int FIXED = 2 * PG_BYTES + 4096 + kMaxKeyBlocks * 12;
     static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
-    static constexpr int NPROD = STAGES_RAW >= 3 ? 3 : (STAGES_RAW >= 2 ? 2 : 1);
-    static constexpr int SPP = (STAGES_RAW < 1 ? 1 : (STAGES_RAW > 6 ? 6 : STAGES_RAW)) / NPROD;
-    static constexpr int STAGES = NPROD * SPP;
+    static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
+    static constexpr int TM_GROUP = 64;  // per warpgroup: S +0, dP +16, gradients +32 (32 columns)
 };
-
-template <class C>
-__device__ __forceinline__ void stage_of(int n, int& st, int& u) {
-    const int k = n / C::NPROD;
-    st = (n % C::NPROD) * C::SPP + k % C::SPP;
-    u = k / C::SPP;
-}
 
 struct Misc {
     // per warpgroup, each used in that group's own item order
@@ -63,6 +65,24 @@ struct Misc {
     uint32_t tmem_slot;
     int abort_flag;
     int n_kb, n_items;
+};
+
+// Walks the items of a CTA in order: key block, group (kb & 1), index within
+// the key block, per-group item and key-block counters (barrier phases).
+struct ItemWalk {
+    int n = -1, kb = 0, w = 0, gi = 0, k = 0, kn = 0;
+    bool last = false;
+    int wk0 = 0, wk1 = 0, wkb0 = 0, wkb1 = 0;  // items / finished key blocks per group
+    __device__ __forceinline__ void next(const int* kitem, const int* kcnt, int n_kb) {
+        n++;
+        while (kb + 1 < n_kb && kitem[kb + 1] <= n) kb++;
+        w = kb & 1;
+        gi = n - kitem[kb];
+        last = 8 * (gi + 1) >= kcnt[kb];
+        k = w ? wk1++ : wk0++;
+        kn = w ? wkb1 : wkb0;
+        if (last) (w ? wkb1 : wkb0)++;
+    }
 };
 
 template <int D>
@@ -75,8 +95,8 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     // __shared__ array by pointer arithmetic so accesses stay shared-space
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stages = sm;
-    unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;  // [warpgroup][P^T, dS^T]
-    Misc* ms = reinterpret_cast<Misc*>(pbuf + 4 * C::PB_BYTES);
+    unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;  // [warpgroup] dS^T / P^T
+    Misc* ms = reinterpret_cast<Misc*>(pbuf + 2 * C::PG_BYTES);
     int* kcnt = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(ms) + 4096);  // per key block: column count
     int* kitem = kcnt + kMaxKeyBlocks;                                                  // first item of the key block
     int* kbeg = kitem + kMaxKeyBlocks;                                                  // first CSC entry of the column
@@ -106,7 +126,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
-            mbar_init(smem_u32(&ms->full[s]), 1);
+            mbar_init(smem_u32(&ms->full[s]), 3);  // one arrival per gather warp
             mbar_init(smem_u32(&ms->empty[s]), 1);
         }
         for (int w = 0; w < 2; w++) {
@@ -151,26 +171,26 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     const uint32_t tbase = ms->tmem_slot;
     const int n_items = ms->n_items;
 
-    if ((warp == 0 || warp == 2 || warp == 3) && (warp == 0 ? 0 : warp - 1) < C::NPROD) {
+    if (warp == 0 || warp == 2 || warp == 3) {
         // ----------------------------------------------------------- gather
-        const int pw = warp == 0 ? 0 : warp - 1;
-        // the query blocks of the next item are loaded while this one is issued
+        // Item n uses stage n % STAGES for the (n / STAGES)-th time. The query
+        // blocks of the next item are located while this one is issued.
+        const int role = warp == 0 ? 0 : warp - 1;
         int kb_walk = 0;
-        auto locate = [&](int n, int& kb, int& gi, int& nv, int& qb) {
+        auto locate = [&](int n, int& kb, int& nv, int& qb) {
             while (kb_walk + 1 < n_kb && kitem[kb_walk + 1] <= n) kb_walk++;
             kb = kb_walk;
-            gi = n - kitem[kb];
+            const int gi = n - kitem[kb];
             nv = min(8, kcnt[kb] - 8 * gi);
             qb = lane < nv ? a.row_idx[((long long)(blockIdx.x + (long long)kb * G) / a.T) * a.T * a.K1 + kbeg[kb] + 8 * gi + lane] : 0;
         };
-        int kb, gi, nv, qb, kb1 = 0, gi1 = 0, nv1 = 0, qb1 = 0;
+        int kb, nv, qb, kb1 = 0, nv1 = 0, qb1 = 0;
         int issued = -1;
-        if (pw < n_items) locate(pw, kb1, gi1, nv1, qb1);
-        for (int n = pw; n < n_items; n += C::NPROD) {
-            kb = kb1; gi = gi1; nv = nv1; qb = qb1;
-            if (n + C::NPROD < n_items) locate(n + C::NPROD, kb1, gi1, nv1, qb1);
-            int st, u;
-            stage_of<C>(n, st, u);
+        if (n_items > 0) locate(0, kb1, nv1, qb1);
+        for (int n = 0; n < n_items; n++) {
+            kb = kb1; nv = nv1; qb = qb1;
+            if (n + 1 < n_items) locate(n + 1, kb1, nv1, qb1);
+            const int st = n % C::STAGES, u = n / C::STAGES;
             bool ok = true;
             if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
@@ -184,139 +204,148 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             }
             unsigned char* sb = stages + st * C::STAGE_BYTES;
             const uint32_t fb = smem_u32(&ms->full[st]);
-            if (lane == 0) mbar_arrive_expect_tx(fb, nv * (2 * C::KB_BYTES + 128) + 2 * C::KB_BYTES);
+            const uint32_t bytes = role == 0 ? 2 * C::KB_BYTES + nv * 128 : nv * C::KB_BYTES;
+            if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
             __syncwarp();
-            if (lane == 0) {
-                const int yk = (int)(slice * a.n + (long long)j * 16);
-                for (int r = 0; r < C::REG; r++) {
-                    tma_load_2d(smem_u32(sb + C::OFF_K + r * 2048), &mk, r * 64, yk, fb);
-                    tma_load_2d(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, yk, fb);
+            const long long tok = slice * a.n + (long long)qb * 16;
+            if (role == 0) {
+                if (lane == 0) {
+                    const int yk = (int)(slice * a.n + (long long)j * 16);
+                    for (int r = 0; r < C::REG; r++) {
+                        tma_load_2d(smem_u32(sb + C::OFF_K + r * 2048), &mk, r * 64, yk, fb);
+                        tma_load_2d(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, yk, fb);
+                    }
                 }
-            }
-            if (lane < nv) {
-                const long long tok = slice * a.n + (long long)qb * 16;
-                for (int r = 0; r < C::REG; r++) {
-                    tma_load_2d(smem_u32(sb + r * 128 * 128 + lane * 2048), &mq, r * 64, (int)tok, fb);
-                    tma_load_2d(smem_u32(sb + C::OFF_DO + r * 128 * 128 + lane * 2048), &mdo, r * 64, (int)tok, fb);
-                }
-                bulk_load(smem_u32(sb + C::OFF_LD + lane * 128), a.Dbuf + 2 * tok, 128, fb);
+                if (lane < nv) bulk_load(smem_u32(sb + C::OFF_LD + lane * 128), a.Dbuf + 2 * tok, 128, fb);
+            } else if (lane < nv) {
+                const int off = role == 1 ? 0 : C::OFF_DO;
+                const CUtensorMap* map = role == 1 ? &mq : &mdo;
+                for (int r = 0; r < C::REG; r++)
+                    tma_load_2d(smem_u32(sb + off + r * 128 * 128 + lane * 2048), map, r * 64, (int)tok, fb);
             }
             issued = n;
         }
+        // copies still in flight must land before the CTA exits
         if (lane == 0)
-            for (int n = issued; n >= 0 && n > issued - C::NPROD * C::SPP; n -= C::NPROD) {
-                int st, u;
-                stage_of<C>(n, st, u);
+            for (int n = issued; n >= 0 && n > issued - C::STAGES; n--) {
+                const int st = n % C::STAGES, u = n / C::STAGES;
                 for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->full[st]), u & 1); it++) {
                 }
             }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        // The whole warp runs the issue loop: lane 0 waits and broadcasts the
-        // result; MMAs and commits are issued by one lane elected inside the
-        // asm (a divergent branch around tcgen05.mma slows each issue).
-        {
-            auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
-                int ok = 1;
-                if (lane == 0) ok = mbar_wait(smem_u32(bar), parity, abort_flag, a.status) ? 1 : 0;
-                return __shfl_sync(0xffffffffu, ok, 0) != 0;
-            };
-            constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
-            constexpr uint32_t idG = idesc_bf16(D, 16, 1, 0);
-            const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);         // K-major
-            const uint64_t dMN = desc_sw128(smem_u32(stages), 128 * 128, 1024);  // stacks as MN-major
-            const uint64_t dPB = desc_sw128(smem_u32(pbuf), 16, 1024);
-            // Item n belongs to the warpgroup of its key block (kb & 1); k is its
-            // index within that group's items, kn its count of non-empty key
-            // blocks before this one. Per-group barriers see their phases in
-            // that group's order, so no wait can alias an older phase.
-            int wk[2] = {0, 0}, wkb[2] = {0, 0};
-            struct Item { int n, w, k, kn, gi; bool last; };
-            auto issue_S = [&](const Item& it) -> bool {
-                int st, u;
-                stage_of<C>(it.n, st, u);
-                if (!wait1(&ms->full[st], u & 1)) return false;
-                if (it.k >= 1 && !wait1(&ms->s_free[it.w], (it.k - 1) & 1))
-                    return false;
-                if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w]));
-                tc_fence_after();
-                const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ks++) {
-                    const uint32_t qoff = (ks / 4) * 128 * 128 + (ks % 4) * 32;
-                    const uint32_t koff = (ks / 4) * 2048 + (ks % 4) * 32;
-                    mma_bf16_warp(tbase + it.w * 32, dKm + ((s0 + qoff) >> 4), dKm + ((s0 + C::OFF_K + koff) >> 4), idS,
-                             ks > 0);
-                    mma_bf16_warp(tbase + it.w * 32 + 16, dKm + ((s0 + C::OFF_DO + qoff) >> 4),
-                             dKm + ((s0 + C::OFF_V + koff) >> 4), idS, ks > 0);
-                }
-                mma_commit_warp(smem_u32(&ms->s_full[it.w]));
-                return true;
-            };
-            auto issue_G = [&](const Item& it) -> bool {
-                int st, u;
-                stage_of<C>(it.n, st, u);
-                if (!wait1(&ms->p_full[it.w], it.k & 1)) return false;
-                // the accumulators are free once the previous key block's epilogue read them
-                if (it.gi == 0 && it.kn >= 1 &&
-                    !wait1(&ms->acc_free[it.w], (it.kn - 1) & 1))
-                    return false;
-                tc_fence_after();
-                const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
-                const uint32_t pb = (uint32_t)(it.w * 2 * C::PB_BYTES);
-#pragma unroll
-                for (int ks = 0; ks < 8; ks++) {
-                    const uint32_t boff = pb + (ks / 4) * 2048 + (ks % 4) * 32;
-                    const uint32_t acc = (it.gi > 0 || ks > 0) ? 1u : 0u;
-                    mma_bf16_warp(tbase + 64 + it.w * 32 + 16, dMN + ((s0 + C::OFF_DO + ks * 2048) >> 4), dPB + (boff >> 4),
-                             idG, acc);
-                    mma_bf16_warp(tbase + 64 + it.w * 32, dMN + ((s0 + ks * 2048) >> 4), dPB + ((boff + C::PB_BYTES) >> 4),
-                             idG, acc);
-                }
-                mma_commit_warp(smem_u32(&ms->p_free[it.w]));
-                mma_commit_warp(smem_u32(&ms->empty[st]));
-                if (it.last) mma_commit_warp(smem_u32(&ms->acc_full[it.w]));
-                return true;
-            };
-            int kb = 0;
-            bool ok = true, have_pending = false;
-            Item pending{};
-            for (int n = 0; ok && n < n_items; n++) {
-                while (kb + 1 < n_kb && kitem[kb + 1] <= n) kb++;
-                Item it;
-                it.n = n;
-                it.w = kb & 1;
-                it.gi = n - kitem[kb];
-                it.last = 8 * (it.gi + 1) >= kcnt[kb];
-                it.k = wk[it.w]++;
-                it.kn = wkb[it.w];
-                if (it.last) wkb[it.w]++;
-                // S of this item goes ahead of the previous item's gradient MMAs
-                // when the two belong to different warpgroups
-                if (have_pending && pending.w == it.w) {
-                    ok = issue_G(pending);
-                    have_pending = false;
-                }
-                if (ok) ok = issue_S(it);
-                if (ok && have_pending) ok = issue_G(pending);
-                pending = it;
-                have_pending = true;
-            }
-            if (ok && have_pending) issue_G(pending);
-            mma_commit_warp(smem_u32(&ms->drain));
-            if (lane == 0)
-                for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
-                }
+        constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
+        constexpr uint32_t idG = D == 64 ? idesc_bf16(128, 32, 1, 0) : idesc_bf16(D, 16, 1, 0);
+        const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);         // K-major
+        const uint64_t dMN = desc_sw128(smem_u32(stages), 128 * 128, 1024);  // stacks as MN-major
+        const uint64_t dPB = desc_sw128(smem_u32(pbuf), 16, 1024);
+        ItemWalk ws, wg;  // next item of the S stream and of the gradient stream
+        if (n_items > 0) {
+            ws.next(kitem, kcnt, n_kb);
+            wg.next(kitem, kcnt, n_kb);
         }
+        auto s_ready = [&](const ItemWalk& it) -> bool {
+            const int st = it.n % C::STAGES, u = it.n / C::STAGES;
+            return mbar_test(smem_u32(&ms->full[st]), u & 1) &&
+                   (it.k == 0 || mbar_test(smem_u32(&ms->s_free[it.w]), (it.k - 1) & 1));
+        };
+        auto g_ready = [&](const ItemWalk& it) -> bool {
+            // the accumulators are free once the previous key block's epilogue read them
+            return mbar_test(smem_u32(&ms->p_full[it.w]), it.k & 1) &&
+                   (it.gi > 0 || it.kn == 0 || mbar_test(smem_u32(&ms->acc_free[it.w]), (it.kn - 1) & 1));
+        };
+        auto issue_S = [&](const ItemWalk& it) {
+            const int st = it.n % C::STAGES;
+            if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w]));  // the group may read the stage
+            tc_fence_after();
+            const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
+            const uint32_t tg = tbase + it.w * C::TM_GROUP;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ks++) {
+                const uint32_t qoff = (ks / 4) * 128 * 128 + (ks % 4) * 32;
+                const uint32_t koff = (ks / 4) * 2048 + (ks % 4) * 32;
+                mma_bf16_warp(tg, dKm + ((s0 + qoff) >> 4), dKm + ((s0 + C::OFF_K + koff) >> 4), idS, ks > 0);
+                mma_bf16_warp(tg + 16, dKm + ((s0 + C::OFF_DO + qoff) >> 4), dKm + ((s0 + C::OFF_V + koff) >> 4),
+                              idS, ks > 0);
+            }
+            mma_commit_warp(smem_u32(&ms->s_full[it.w]));
+        };
+        auto issue_G = [&](const ItemWalk& it) {
+            const int st = it.n % C::STAGES;
+            tc_fence_after();
+            const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
+            const uint32_t pg = (uint32_t)(it.w * C::PG_BYTES);
+            const uint32_t tg = tbase + it.w * C::TM_GROUP + 32;
+#pragma unroll
+            for (int ks = 0; ks < 8; ks++) {
+                const uint32_t boff = pg + (ks / 4) * 4096 + (ks % 4) * 32;
+                const uint32_t acc = (it.gi > 0 || ks > 0) ? 1u : 0u;
+                if (D == 64) {
+                    // rows 0-63 Q^T, rows 64-127 dO^T (the dO stack is QS_BYTES on,
+                    // the descriptor's M-chunk stride); columns 0-15 dS, 16-31 P
+                    mma_bf16_warp(tg, dMN + ((s0 + ks * 2048) >> 4), dPB + (boff >> 4), idG, acc);
+                } else {
+                    mma_bf16_warp(tg, dMN + ((s0 + ks * 2048) >> 4), dPB + (boff >> 4), idG, acc);
+                    mma_bf16_warp(tg + 16, dMN + ((s0 + C::OFF_DO + ks * 2048) >> 4), dPB + ((boff + 2048) >> 4), idG,
+                                  acc);
+                }
+            }
+            mma_commit_warp(smem_u32(&ms->p_free[it.w]));
+            mma_commit_warp(smem_u32(&ms->empty[st]));
+            if (it.last) mma_commit_warp(smem_u32(&ms->acc_full[it.w]));
+        };
+        // out of order between the two in-order streams; idle polls bounded
+        int nS = 0, nG = 0, idle = 0;
+        while (nG < n_items) {
+            int act = 0;
+            if (lane == 0) {
+                if (nG < nS && g_ready(wg)) act = 2;
+                else if (nS < n_items && s_ready(ws)) act = 1;
+            }
+            act = __shfl_sync(0xffffffffu, act, 0);
+            if (act == 1) {
+                issue_S(ws);
+                if (++nS < n_items) ws.next(kitem, kcnt, n_kb);
+                idle = 0;
+            } else if (act == 2) {
+                issue_G(wg);
+                if (++nG < n_items) wg.next(kitem, kcnt, n_kb);
+                idle = 0;
+            } else {
+                int stop = 0;
+                if (lane == 0) {
+                    if (++idle >= kSpinLimit) {
+                        *abort_flag = 1;
+                        set_status(a.status, LLSA_ERR_TIMEOUT);
+                        stop = 1;
+                    } else if ((idle & 63) == 0 && *abort_flag) {
+                        stop = 1;
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            }
+        }
+        // no MMA may be in flight when TMEM is released
+        mma_commit_warp(smem_u32(&ms->drain));
+        if (lane == 0)
+            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+            }
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------ P, dS per query row; epilogue
         const int w = (warp - 4) >> 2, qr = warp & 3;
         const int tq = threadIdx.x - 128 * (1 + w);  // query row of the stack = TMEM lane
         const uint32_t lanes = (uint32_t)(qr * 32) << 16;
+        const uint32_t tg = tbase + w * C::TM_GROUP + lanes;
         const float sc = a.scale, scl2 = a.scale * kLog2e;
-        const int dd = D == 64 ? 16 * qr + lane : 32 * qr + lane;
-        const bool valid = D == 64 ? lane < 16 : true;
+        // epilogue rows: for d = 64, warps 0-1 of the group hold dk^T rows and
+        // warps 2-3 dv^T rows (TMEM lanes 0-63 / 64-127); for d = 128 every
+        // warp holds 32 rows of both
+        const bool is_k = D == 64 ? qr < 2 : true;
+        const int dd = D == 64 ? 32 * (qr & 1) + lane : 32 * qr + lane;
+        unsigned char* PG = pbuf + w * C::PG_BYTES;
+        unsigned char* pb = PG + (tq >> 6) * 4096 + (tq & 7) * 2;
+        const int chk = (tq & 63) >> 3;
         int acc_phase = 0, k = 0;
         for (int kb = w; kb < n_kb; kb += 2) {
             const long long g = blockIdx.x + (long long)kb * G;
@@ -325,23 +354,21 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             const int cnt = kcnt[kb], items = (cnt + 7) / 8;
             // pooled-level gradients above this key block, fetched before its items
             float fk = 0.f, fv = 0.f;
-            if (valid) {
+            {
                 long long span = a.B;
                 int anc = j;
                 for (int l = 1; l <= a.Le; l++) {
                     const long long off = (slice * a.P + a.lv.row_offset[l] + anc) * (long long)D + dd;
                     const float inv = 1.0f / (float)span;
-                    fk = fmaf(a.dKc[off], inv, fk);
-                    fv = fmaf(a.dVc[off], inv, fv);
+                    if (is_k) fk = fmaf(a.dKc[off], inv, fk);
+                    if (D == 128 || !is_k) fv = fmaf(a.dVc[off], inv, fv);
                     span *= a.B;
                     anc /= a.B;
                 }
             }
             for (int gi = 0; gi < items; gi++, k++) {
                 const int n = kitem[kb] + gi;
-                int st, u;
-                stage_of<C>(n, st, u);
-                const unsigned char* sb = stages + st * C::STAGE_BYTES;
+                const unsigned char* sb = stages + (n % C::STAGES) * C::STAGE_BYTES;
                 const bool row_ok = tq < 16 * min(8, cnt - 8 * gi);
                 // waits return at once after a timeout; the group keeps walking
                 mbar_wait(smem_u32(&ms->q_ready[w]), k & 1, abort_flag, a.status);
@@ -350,15 +377,12 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 mbar_wait(smem_u32(&ms->s_full[w]), k & 1, abort_flag, a.status);
                 tc_fence_after();
                 float s[16], dp[16];
-                tmem_ld16(tbase + lanes + w * 32, s);
-                tmem_ld16(tbase + lanes + w * 32 + 16, dp);
+                tmem_ld16(tg, s);
+                tmem_ld16(tg + 16, dp);
                 tc_fence_before();
                 mbar_arrive(smem_u32(&ms->s_free[w]));
-                // the P / dS operands of this group's previous item must be consumed
+                // the operands of this group's previous item must be consumed
                 if (k >= 1) mbar_wait(smem_u32(&ms->p_free[w]), (k - 1) & 1, abort_flag, a.status);
-                unsigned char* PT = pbuf + w * 2 * C::PB_BYTES;
-                unsigned char* pb = PT + (tq >> 6) * 2048 + (tq & 7) * 2;
-                const int chk = (tq & 63) >> 3;
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
                     float pr = ex2(fmaf(s[c], scl2, -lse2));
@@ -368,8 +392,8 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                         ds = 0.f;
                     }
                     const uint32_t off = c * 128 + ((chk ^ (c & 7)) << 4);
-                    *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(pr);
-                    *reinterpret_cast<__nv_bfloat16*>(pb + C::PB_BYTES + off) = __float2bfloat16_rn(ds);
+                    *reinterpret_cast<__nv_bfloat16*>(pb + off) = __float2bfloat16_rn(ds);
+                    *reinterpret_cast<__nv_bfloat16*>(pb + 2048 + off) = __float2bfloat16_rn(pr);
                 }
                 fence_async_smem();
                 mbar_arrive(smem_u32(&ms->p_full[w]));
@@ -380,21 +404,29 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 mbar_wait(smem_u32(&ms->acc_full[w]), acc_phase & 1, abort_flag, a.status);
                 acc_phase++;
                 tc_fence_after();
-                tmem_ld16(tbase + lanes + 64 + w * 32, kk);
-                tmem_ld16(tbase + lanes + 64 + w * 32 + 16, vv);
+                if (D == 64) {
+                    tmem_ld16(tg + 32 + (is_k ? 0 : 16), kk);
+#pragma unroll
+                    for (int c = 0; c < 16; c++) vv[c] = kk[c];
+                } else {
+                    tmem_ld16(tg + 32, kk);
+                    tmem_ld16(tg + 48, vv);
+                }
                 tc_fence_before();
             } else {
 #pragma unroll
                 for (int c = 0; c < 16; c++) kk[c] = vv[c] = 0.f;
             }
-            if (valid) {
-                __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + (slice * a.n + (long long)j * 16) * D + dd;
-                __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + (slice * a.n + (long long)j * 16) * D + dd;
+            const long long row0 = (slice * a.n + (long long)j * 16) * D + dd;
+            if (is_k) {
+                __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + row0;
 #pragma unroll
-                for (int c = 0; c < 16; c++) {
-                    dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
-                    dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
-                }
+                for (int c = 0; c < 16; c++) dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+            }
+            if (D == 128 || !is_k) {
+                __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + row0;
+#pragma unroll
+                for (int c = 0; c < 16; c++) dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
             }
             if (items > 0) mbar_arrive(smem_u32(&ms->acc_free[w]));
         }
@@ -412,9 +444,7 @@ int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaS
     using C = Cfg<D>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(Misc) <= 4096, "misc block");
-    // the MMA thread holds one item's gradient MMAs back while it issues the
-    // next item's S; that needs a second stage
-    static_assert(C::STAGES >= 2, "two stages at least");
+    static_assert(C::STAGES >= 1, "one stage at least");
     cudaFuncSetAttribute(bwd_dkv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
