@@ -44,6 +44,44 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def csrc_digest() -> str:
+    """Digest of the CUDA sources and the C header: a recorded ncu figure
+    applies only to the build it was taken on."""
+    import hashlib
+    h = hashlib.sha256()
+    for d in ("hierarchical_sparse_attention_mean_gb300/csrc", "include"):
+        for f in sorted(os.listdir(os.path.join(ROOT, d))):
+            if f.endswith((".cu", ".cuh", ".h")):
+                rel = os.path.join(d, f)
+                h.update(rel.encode())
+                with open(os.path.join(ROOT, rel), "rb") as fh:
+                    h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    of `kernel` from the committed ncu summary of this workload, or None when
+    the summary is missing or was taken on other sources."""
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    digest, table = None, {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("csrc digest:"):
+                digest = line.split(":", 1)[1].strip().strip("`")
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) >= 4 and cells[0].startswith("`"):
+                try:
+                    table[cells[0].strip("`")] = float(cells[3].replace(",", ""))
+                except ValueError:
+                    pass
+    if digest != csrc_digest():
+        return None
+    return table.get(kernel)
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -73,7 +111,9 @@ def work_model(w: synth.Workload, s) -> dict:
         "kernels": {
             "pool_chunk": (3 * tok + 3 * bh * P * d * 4, 0),
             "fwd": (4 * tok + bh * n * 4, 4 * d * pairs),
-            "bwd_dq": (4 * tok + bh * n * 8, 6 * d * pairs),
+            # reads Q, dO, o, lse and the gathered K, V (each once from HBM);
+            # writes dq, the (lse, D) pairs and the pooled-level partials
+            "bwd_dq": (6 * tok + bh * n * 12 + 2 * bh * s.n_blocks * s.enrich_levels * d * 4, 6 * d * pairs),
             "bwd_dkv": (6 * tok + bh * n * 8, 8 * d * fine_pairs),
             "transpose": (4 * bh * s.n_blocks * s.topk_level[1] * 3, 0),
             "select_level": (0, 2 * d * scored * bh),
@@ -237,8 +277,9 @@ def run_llsa(args, ws, rank, local):
     avg_ms = per[dom][0] / per[dom][1]
     tensor_path = dom in llsa_tensor_kernels(records)
     roof = kernel_bound(dom, avg_ms, work, peaks, tensor_path)
+    traffic = args.traffic if args.traffic is not None else recorded_traffic(w.name, dom)
     roof.update({"kernel": dom, "avg_launch_ms": round(avg_ms, 4), "peak_source": peak_src,
-                 "traffic": args.traffic})
+                 "traffic": traffic, "traffic_source": "ncu dram bytes per launch, same sources" if traffic else None})
 
     # ---- end to end through host buffers: every step uploads its inputs from
     # pinned host memory and downloads its results (o, dq, dk, dv). Inputs and
