@@ -49,19 +49,26 @@ struct Cfg {
     static constexpr int OFF_DO = QS_BYTES, OFF_K = 2 * QS_BYTES, OFF_V = OFF_K + KB_BYTES;
     static constexpr int OFF_LD = OFF_V + KB_BYTES;
     static constexpr int STAGE_BYTES = OFF_LD + 1024;
-    // per warpgroup: dS^T and P^T of one item as K-major operands, interleaved
-    // per 64 rows (dS^T chunk c at c * 4096, P^T chunk c at c * 4096 + 2048)
+    // per warpgroup and buffer: dS^T and P^T of one item as K-major operands,
+    // interleaved per 64 rows (dS^T chunk c at c * 4096, P^T chunk c at +2048)
     static constexpr int PG_BYTES = 8192;
-    static constexpr int FIXED = 2 * PG_BYTES + 4096 + kMaxKeyBlocks * 12;
+    static constexpr int FIXED = 4 * PG_BYTES + 4096 + kMaxKeyBlocks * 12;
     static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
-    static constexpr int TM_GROUP = 64;  // per warpgroup: S +0, dP +16, gradients +32 (32 columns)
+    // per warpgroup: two S/dP buffers (+0, +32: S, then dP 16 columns on;
+    // alternate items of the group) and two gradient accumulators (+64, +96:
+    // 32 columns each, alternate key blocks of the group)
+    static constexpr int TM_GROUP = 128;
 };
 
 struct Misc {
     // per warpgroup, each used in that group's own item order
-    uint64_t full[6], empty[6], q_ready[2], s_full[2], s_free[2], p_full[2], p_free[2], acc_full[2], acc_free[2], drain;
+    // [group][buffer]: item buffers alternate with the group's items,
+    // accumulators with its key blocks
+    uint64_t full[6], empty[6];
+    uint64_t q_ready[2][2], s_full[2][2], s_free[2][2], p_full[2][2], p_free[2][2];
+    uint64_t acc_full[2][2], acc_free[2][2], drain;
     uint32_t tmem_slot;
     int abort_flag;
     int n_kb, n_items;
@@ -95,8 +102,8 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     // __shared__ array by pointer arithmetic so accesses stay shared-space
     unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* stages = sm;
-    unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;  // [warpgroup] dS^T / P^T
-    Misc* ms = reinterpret_cast<Misc*>(pbuf + 2 * C::PG_BYTES);
+    unsigned char* pbuf = stages + C::STAGES * C::STAGE_BYTES;  // [warpgroup][buffer] dS^T / P^T
+    Misc* ms = reinterpret_cast<Misc*>(pbuf + 4 * C::PG_BYTES);
     int* kcnt = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(ms) + 4096);  // per key block: column count
     int* kitem = kcnt + kMaxKeyBlocks;                                                  // first item of the key block
     int* kbeg = kitem + kMaxKeyBlocks;                                                  // first CSC entry of the column
@@ -130,13 +137,15 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             mbar_init(smem_u32(&ms->empty[s]), 1);
         }
         for (int w = 0; w < 2; w++) {
-            mbar_init(smem_u32(&ms->q_ready[w]), 1);
-            mbar_init(smem_u32(&ms->s_full[w]), 1);
-            mbar_init(smem_u32(&ms->s_free[w]), 128);
-            mbar_init(smem_u32(&ms->p_full[w]), 128);
-            mbar_init(smem_u32(&ms->p_free[w]), 1);
-            mbar_init(smem_u32(&ms->acc_full[w]), 1);
-            mbar_init(smem_u32(&ms->acc_free[w]), 128);
+            for (int b = 0; b < 2; b++) {
+                mbar_init(smem_u32(&ms->q_ready[w][b]), 1);
+                mbar_init(smem_u32(&ms->s_full[w][b]), 1);
+                mbar_init(smem_u32(&ms->s_free[w][b]), 128);
+                mbar_init(smem_u32(&ms->p_full[w][b]), 128);
+                mbar_init(smem_u32(&ms->p_free[w][b]), 1);
+                mbar_init(smem_u32(&ms->acc_full[w][b]), 1);
+                mbar_init(smem_u32(&ms->acc_free[w][b]), 128);
+            }
         }
         mbar_init(smem_u32(&ms->drain), 1);
         ms->abort_flag = 0;
@@ -164,7 +173,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             ms->n_items = carry;
         }
     }
-    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), 128);
+    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), 256);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -247,19 +256,21 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         auto s_ready = [&](const ItemWalk& it) -> bool {
             const int st = it.n % C::STAGES, u = it.n / C::STAGES;
             return mbar_test(smem_u32(&ms->full[st]), u & 1) &&
-                   (it.k == 0 || mbar_test(smem_u32(&ms->s_free[it.w]), (it.k - 1) & 1));
+                   (it.k < 2 || mbar_test(smem_u32(&ms->s_free[it.w][it.k & 1]), ((it.k >> 1) - 1) & 1));
         };
         auto g_ready = [&](const ItemWalk& it) -> bool {
-            // the accumulators are free once the previous key block's epilogue read them
-            return mbar_test(smem_u32(&ms->p_full[it.w]), it.k & 1) &&
-                   (it.gi > 0 || it.kn == 0 || mbar_test(smem_u32(&ms->acc_free[it.w]), (it.kn - 1) & 1));
+            // an accumulator is free once the epilogue of the group's key block
+            // before last (the previous user of the same accumulator) read it
+            return mbar_test(smem_u32(&ms->p_full[it.w][it.k & 1]), (it.k >> 1) & 1) &&
+                   (it.gi > 0 || it.kn < 2 ||
+                    mbar_test(smem_u32(&ms->acc_free[it.w][it.kn & 1]), ((it.kn >> 1) - 1) & 1));
         };
         auto issue_S = [&](const ItemWalk& it) {
             const int st = it.n % C::STAGES;
-            if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w]));  // the group may read the stage
+            if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w][it.k & 1]));  // the group may read the stage
             tc_fence_after();
             const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
-            const uint32_t tg = tbase + it.w * C::TM_GROUP;
+            const uint32_t tg = tbase + it.w * C::TM_GROUP + (it.k & 1) * 32;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ks++) {
                 const uint32_t qoff = (ks / 4) * 128 * 128 + (ks % 4) * 32;
@@ -268,14 +279,14 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 mma_bf16_warp(tg + 16, dKm + ((s0 + C::OFF_DO + qoff) >> 4), dKm + ((s0 + C::OFF_V + koff) >> 4),
                               idS, ks > 0);
             }
-            mma_commit_warp(smem_u32(&ms->s_full[it.w]));
+            mma_commit_warp(smem_u32(&ms->s_full[it.w][it.k & 1]));
         };
         auto issue_G = [&](const ItemWalk& it) {
             const int st = it.n % C::STAGES;
             tc_fence_after();
             const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
-            const uint32_t pg = (uint32_t)(it.w * C::PG_BYTES);
-            const uint32_t tg = tbase + it.w * C::TM_GROUP + 32;
+            const uint32_t pg = (uint32_t)((it.w * 2 + (it.k & 1)) * C::PG_BYTES);
+            const uint32_t tg = tbase + it.w * C::TM_GROUP + 64 + (it.kn & 1) * 32;
 #pragma unroll
             for (int ks = 0; ks < 8; ks++) {
                 const uint32_t boff = pg + (ks / 4) * 4096 + (ks % 4) * 32;
@@ -290,9 +301,9 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                                   acc);
                 }
             }
-            mma_commit_warp(smem_u32(&ms->p_free[it.w]));
+            mma_commit_warp(smem_u32(&ms->p_free[it.w][it.k & 1]));
             mma_commit_warp(smem_u32(&ms->empty[st]));
-            if (it.last) mma_commit_warp(smem_u32(&ms->acc_full[it.w]));
+            if (it.last) mma_commit_warp(smem_u32(&ms->acc_full[it.w][it.kn & 1]));
         };
         // out of order between the two in-order streams; idle polls bounded
         int nS = 0, nG = 0, idle = 0;
@@ -343,26 +354,76 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         // warp holds 32 rows of both
         const bool is_k = D == 64 ? qr < 2 : true;
         const int dd = D == 64 ? 32 * (qr & 1) + lane : 32 * qr + lane;
-        unsigned char* PG = pbuf + w * C::PG_BYTES;
-        unsigned char* pb = PG + (tq >> 6) * 4096 + (tq & 7) * 2;
+        unsigned char* pb0 = pbuf + w * 2 * C::PG_BYTES + (tq >> 6) * 4096 + (tq & 7) * 2;
         const int chk = (tq & 63) >> 3;
-        int acc_phase = 0, k = 0;
+        int kn = 0, k = 0;  // key blocks with items / items of this group so far
+        // The epilogue of a key block runs after the first item of the group's
+        // next key block (its accumulator is the other one), so its wait on
+        // the last gradient MMA and its stores overlap that item.
+        bool pend = false, pacc = false;
+        long long pslice = 0;
+        int pj = 0, pkn = 0;
+        float prk[4], prv[4];
+        auto epilogue = [&]() {
+            // dk = scale * acc + pooled fold, dv = acc + pooled fold
+            float kk[16], vv[16];
+            if (pacc) {
+                mbar_wait(smem_u32(&ms->acc_full[w][pkn & 1]), (pkn >> 1) & 1, abort_flag, a.status);
+                tc_fence_after();
+                const uint32_t ta = tg + 64 + (pkn & 1) * 32;
+                if (D == 64) {
+                    tmem_ld16(ta + (is_k ? 0 : 16), kk);
+#pragma unroll
+                    for (int c = 0; c < 16; c++) vv[c] = kk[c];
+                } else {
+                    tmem_ld16(ta, kk);
+                    tmem_ld16(ta + 16, vv);
+                }
+                tc_fence_before();
+                mbar_arrive(smem_u32(&ms->acc_free[w][pkn & 1]));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 16; c++) kk[c] = vv[c] = 0.f;
+            }
+            float fk = 0.f, fv = 0.f;
+            long long span = a.B;  // B^l
+#pragma unroll
+            for (int l = 0; l < 4; l++) {
+                const float inv = 1.0f / (float)span;
+                fk = fmaf(prk[l], inv, fk);
+                fv = fmaf(prv[l], inv, fv);
+                span *= a.B;
+            }
+            const long long row0 = (pslice * a.n + (long long)pj * 16) * D + dd;
+            if (is_k) {
+                __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + row0;
+#pragma unroll
+                for (int c = 0; c < 16; c++) dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+            }
+            if (D == 128 || !is_k) {
+                __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + row0;
+#pragma unroll
+                for (int c = 0; c < 16; c++) dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
+            }
+        };
         for (int kb = w; kb < n_kb; kb += 2) {
             const long long g = blockIdx.x + (long long)kb * G;
             const long long slice = g / a.T;
             const int j = (int)(g - slice * a.T);
             const int cnt = kcnt[kb], items = (cnt + 7) / 8;
-            // pooled-level gradients above this key block, fetched before its items
-            float fk = 0.f, fv = 0.f;
+            // pooled-level gradients above this key block: loaded before its
+            // items, combined only in its epilogue so the loads' latency hides
+            float rk[4], rv[4];
             {
-                long long span = a.B;
                 int anc = j;
-                for (int l = 1; l <= a.Le; l++) {
-                    const long long off = (slice * a.P + a.lv.row_offset[l] + anc) * (long long)D + dd;
-                    const float inv = 1.0f / (float)span;
-                    if (is_k) fk = fmaf(a.dKc[off], inv, fk);
-                    if (D == 128 || !is_k) fv = fmaf(a.dVc[off], inv, fv);
-                    span *= a.B;
+#pragma unroll
+                for (int l = 0; l < 4; l++) {
+                    rk[l] = rv[l] = 0.f;
+                    if (l < a.Le) {
+                        const long long off = (slice * a.P + a.lv.row_offset[l + 1] + anc) * (long long)D + dd;
+                        if (is_k) rk[l] = a.dKc[off];
+                        if (D == 128 || !is_k) rv[l] = a.dVc[off];
+                    }
                     anc /= a.B;
                 }
             }
@@ -371,18 +432,21 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 const unsigned char* sb = stages + (n % C::STAGES) * C::STAGE_BYTES;
                 const bool row_ok = tq < 16 * min(8, cnt - 8 * gi);
                 // waits return at once after a timeout; the group keeps walking
-                mbar_wait(smem_u32(&ms->q_ready[w]), k & 1, abort_flag, a.status);
+                const int b = k & 1;
+                const uint32_t ph = (uint32_t)(k >> 1) & 1;
+                mbar_wait(smem_u32(&ms->q_ready[w][b]), ph, abort_flag, a.status);
                 const float2 ld = *reinterpret_cast<const float2*>(sb + C::OFF_LD + tq * 8);  // (lse, D)
                 const float lse2 = ld.x * kLog2e, Dq = ld.y;
-                mbar_wait(smem_u32(&ms->s_full[w]), k & 1, abort_flag, a.status);
+                mbar_wait(smem_u32(&ms->s_full[w][b]), ph, abort_flag, a.status);
                 tc_fence_after();
                 float s[16], dp[16];
-                tmem_ld16(tg, s);
-                tmem_ld16(tg + 16, dp);
+                tmem_ld16(tg + b * 32, s);
+                tmem_ld16(tg + b * 32 + 16, dp);
                 tc_fence_before();
-                mbar_arrive(smem_u32(&ms->s_free[w]));
-                // the operands of this group's previous item must be consumed
-                if (k >= 1) mbar_wait(smem_u32(&ms->p_free[w]), (k - 1) & 1, abort_flag, a.status);
+                mbar_arrive(smem_u32(&ms->s_free[w][b]));
+                // the operands of this group's item before last (same buffer) must be consumed
+                if (k >= 2) mbar_wait(smem_u32(&ms->p_free[w][b]), ph ^ 1u, abort_flag, a.status);
+                unsigned char* pb = pb0 + b * C::PG_BYTES;
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
                     float pr = ex2(fmaf(s[c], scl2, -lse2));
@@ -396,46 +460,35 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                     *reinterpret_cast<__nv_bfloat16*>(pb + 2048 + off) = __float2bfloat16_rn(pr);
                 }
                 fence_async_smem();
-                mbar_arrive(smem_u32(&ms->p_full[w]));
-            }
-            // epilogue: dk = scale * acc + pooled fold, dv = acc + pooled fold
-            float kk[16], vv[16];
-            if (items > 0) {
-                mbar_wait(smem_u32(&ms->acc_full[w]), acc_phase & 1, abort_flag, a.status);
-                acc_phase++;
-                tc_fence_after();
-                if (D == 64) {
-                    tmem_ld16(tg + 32 + (is_k ? 0 : 16), kk);
-#pragma unroll
-                    for (int c = 0; c < 16; c++) vv[c] = kk[c];
-                } else {
-                    tmem_ld16(tg + 32, kk);
-                    tmem_ld16(tg + 48, vv);
+                mbar_arrive(smem_u32(&ms->p_full[w][b]));
+                if (gi == 0 && pend) {
+                    epilogue();
+                    pend = false;
                 }
-                tc_fence_before();
-            } else {
-#pragma unroll
-                for (int c = 0; c < 16; c++) kk[c] = vv[c] = 0.f;
             }
-            const long long row0 = (slice * a.n + (long long)j * 16) * D + dd;
-            if (is_k) {
-                __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + row0;
-#pragma unroll
-                for (int c = 0; c < 16; c++) dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+            if (pend) {  // no item to overlap with
+                epilogue();
+                pend = false;
             }
-            if (D == 128 || !is_k) {
-                __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + row0;
+            pend = true;
+            pacc = items > 0;
+            pslice = slice;
+            pj = j;
+            pkn = kn;
 #pragma unroll
-                for (int c = 0; c < 16; c++) dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
+            for (int l = 0; l < 4; l++) {
+                prk[l] = rk[l];
+                prv[l] = rv[l];
             }
-            if (items > 0) mbar_arrive(smem_u32(&ms->acc_free[w]));
+            if (items > 0) kn++;
         }
+        if (pend) epilogue();
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tbase, 128);
+        tmem_dealloc(tbase, 256);
     }
 }
 

@@ -241,3 +241,35 @@ def test_deterministic_across_runs():
     torch.cuda.synchronize()
     for a, c in zip(*outs):
         assert torch.equal(a, c)
+
+
+def test_fine_logits_far_above_pooled_logits():
+    """Keys whose block means cancel (so every pooled key is zero and every
+    pooled logit is its ln B^l bias) against queries that are, on alternate
+    query blocks, large multiples of the keys' direction: there the fine
+    logits exceed the pooled ones by about 70 nats, beyond the range the
+    forward's pooled-logit shift covers, so those blocks take the exact-maximum
+    path while the others keep the shifted one."""
+    n, d, B = 4096, 64, 16
+    w = W("wide", 1, 2, n, d, amplitude=0.5, seed=8)
+    x = synth.make_inputs(w)
+    rng = np.random.default_rng(8)
+    u = rng.standard_normal(d)
+    u /= np.linalg.norm(u)
+    sign = np.where(np.arange(n) % 2 == 0, 1.0, -1.0)        # block means of K are exactly zero
+    big = np.sqrt(80.0 * np.sqrt(d))                           # scale * |q| * |k| = 80 on large blocks
+    cq = np.where((np.arange(n) // B) % 2 == 0, big, 0.3)      # alternate query blocks large / small
+    k = (big * sign)[:, None] * u[None, :]
+    q = cq[:, None] * u[None, :]
+    for s in range(2):
+        x["k"][s] = synth.bf16_round(k.astype(np.float32))
+        x["q"][s] = synth.bf16_round(q.astype(np.float32))
+    # |q|, |k| ~ 25 make dk, dq ~ 25x larger than usual; dO / 32 (exact in bf16)
+    # keeps the gradients on the scale the absolute bf16 tolerance assumes
+    x["dout"] = x["dout"] / 32.0
+    ref = run_oracle(w, x)
+    out, _ = gpu_stage_outputs(w, x, oracle_sel=ref["slices"])
+    assert_close("o", out["o"], ref["o"], "bf16")
+    assert_lse(out["lse"], ref["lse"])
+    for key in ("dq", "dk", "dv"):
+        assert_close(key, out[key], ref[key], "bf16")
