@@ -22,9 +22,8 @@
 //
 // Warp roles: three gather warps split every item's copies (warp 0 K_j, V_j
 // and the (lse, D) rows; warp 2 the Q stack; warp 3 the dO stack) into a ring
-// of stages; warp 1 issues the MMAs out of order between the S stream and the
-// gradient stream (gradient first, as it frees a stage), through an election
-// inside the MMA asm.
+// of stages; warp 1 issues the S stream and warp 12 the gradient stream, each
+// in order with blocking waits, through an election inside the MMA asm.
 #include <algorithm>
 
 #include "attn.h"
@@ -35,7 +34,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 416;  // 13 warps: 3 gather, 2 MMA issuers, 8 in two warpgroups
 constexpr int kSmemBudget = 215 * 1024;
 constexpr int kMaxKeyBlocks = 2048;  // key blocks per CTA (counts kept in shared memory)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,7 +67,7 @@ struct Misc {
     // accumulators with its key blocks
     uint64_t full[6], empty[6];
     uint64_t q_ready[2][2], s_full[2][2], s_free[2][2], p_full[2][2], p_free[2][2];
-    uint64_t acc_full[2][2], acc_free[2][2], drain;
+    uint64_t acc_full[2][2], acc_free[2][2], drain[2];
     uint32_t tmem_slot;
     int abort_flag;
     int n_kb, n_items;
@@ -147,7 +146,8 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 mbar_init(smem_u32(&ms->acc_free[w][b]), 128);
             }
         }
-        mbar_init(smem_u32(&ms->drain), 1);
+        mbar_init(smem_u32(&ms->drain[0]), 1);
+        mbar_init(smem_u32(&ms->drain[1]), 1);
         ms->abort_flag = 0;
         fence_mbar_init();
     }
@@ -241,30 +241,13 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->full[st]), u & 1); it++) {
                 }
             }
-    } else if (warp == 1) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 12) {
+        // ------------------------------------------------------ MMA issuers
         constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
         constexpr uint32_t idG = D == 64 ? idesc_bf16(128, 32, 1, 0) : idesc_bf16(D, 16, 1, 0);
         const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);         // K-major
         const uint64_t dMN = desc_sw128(smem_u32(stages), 128 * 128, 1024);  // stacks as MN-major
         const uint64_t dPB = desc_sw128(smem_u32(pbuf), 16, 1024);
-        ItemWalk ws, wg;  // next item of the S stream and of the gradient stream
-        if (n_items > 0) {
-            ws.next(kitem, kcnt, n_kb);
-            wg.next(kitem, kcnt, n_kb);
-        }
-        auto s_ready = [&](const ItemWalk& it) -> bool {
-            const int st = it.n % C::STAGES, u = it.n / C::STAGES;
-            return mbar_test(smem_u32(&ms->full[st]), u & 1) &&
-                   (it.k < 2 || mbar_test(smem_u32(&ms->s_free[it.w][it.k & 1]), ((it.k >> 1) - 1) & 1));
-        };
-        auto g_ready = [&](const ItemWalk& it) -> bool {
-            // an accumulator is free once the epilogue of the group's key block
-            // before last (the previous user of the same accumulator) read it
-            return mbar_test(smem_u32(&ms->p_full[it.w][it.k & 1]), (it.k >> 1) & 1) &&
-                   (it.gi > 0 || it.kn < 2 ||
-                    mbar_test(smem_u32(&ms->acc_free[it.w][it.kn & 1]), ((it.kn >> 1) - 1) & 1));
-        };
         auto issue_S = [&](const ItemWalk& it) {
             const int st = it.n % C::STAGES;
             if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w][it.k & 1]));  // the group may read the stage
@@ -305,44 +288,38 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             mma_commit_warp(smem_u32(&ms->empty[st]));
             if (it.last) mma_commit_warp(smem_u32(&ms->acc_full[it.w][it.kn & 1]));
         };
-        // out of order between the two in-order streams; idle polls bounded
-        int nS = 0, nG = 0, idle = 0;
-        while (nG < n_items) {
-            int act = 0;
-            if (lane == 0) {
-                if (nG < nS && g_ready(wg)) act = 2;
-                else if (nS < n_items && s_ready(ws)) act = 1;
-            }
-            act = __shfl_sync(0xffffffffu, act, 0);
-            if (act == 1) {
-                issue_S(ws);
-                if (++nS < n_items) ws.next(kitem, kcnt, n_kb);
-                idle = 0;
-            } else if (act == 2) {
-                issue_G(wg);
-                if (++nG < n_items) wg.next(kitem, kcnt, n_kb);
-                idle = 0;
+        // one in-order stream per issuing warp: warp 1 the S stream, warp 12
+        // the gradient stream; each waits on its own barriers, lane 0 waiting
+        // and broadcasting the outcome
+        auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(bar), parity, abort_flag, a.status) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, ok, 0) != 0;
+        };
+        ItemWalk it;
+        const bool s_role = warp == 1;
+        for (int n = 0; n < n_items; n++) {
+            it.next(kitem, kcnt, n_kb);
+            const int st = it.n % C::STAGES, u = it.n / C::STAGES;
+            if (s_role) {
+                if (!wait1(&ms->full[st], u & 1)) break;
+                if (it.k >= 2 && !wait1(&ms->s_free[it.w][it.k & 1], ((it.k >> 1) - 1) & 1)) break;
+                issue_S(it);
             } else {
-                int stop = 0;
-                if (lane == 0) {
-                    if (++idle >= kSpinLimit) {
-                        *abort_flag = 1;
-                        set_status(a.status, LLSA_ERR_TIMEOUT);
-                        stop = 1;
-                    } else if ((idle & 63) == 0 && *abort_flag) {
-                        stop = 1;
-                    }
-                }
-                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+                // an accumulator is free once the epilogue of the group's key
+                // block before last (its previous user) read it
+                if (!wait1(&ms->p_full[it.w][it.k & 1], (it.k >> 1) & 1)) break;
+                if (it.gi == 0 && it.kn >= 2 && !wait1(&ms->acc_free[it.w][it.kn & 1], ((it.kn >> 1) - 1) & 1)) break;
+                issue_G(it);
             }
         }
-        // no MMA may be in flight when TMEM is released
-        mma_commit_warp(smem_u32(&ms->drain));
+        // no MMA of this warp may be in flight when TMEM is released
+        mma_commit_warp(smem_u32(&ms->drain[s_role ? 0 : 1]));
         if (lane == 0)
-            for (int it = 0; it < kSpinLimit && !mbar_try(smem_u32(&ms->drain), 0); it++) {
+            for (int x = 0; x < kSpinLimit && !mbar_try(smem_u32(&ms->drain[s_role ? 0 : 1]), 0); x++) {
             }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 12) {
         // ------------------------------------------ P, dS per query row; epilogue
         const int w = (warp - 4) >> 2, qr = warp & 3;
         const int tq = threadIdx.x - 128 * (1 + w);  // query row of the stack = TMEM lane
