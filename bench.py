@@ -343,6 +343,8 @@ def run_llsa(args, ws, rank, local):
         raise RuntimeError(f"device status {status} after the timed region")
 
     value = ws * work["step_flops"] / (ms_step * 1e-3) / 1e12
+    stage_gbs = {k: round(work["kernels"][k][0] / (stage_ms[k] * 1e-3) / 1e9, 1)
+                 for k in ("pool_chunk", "transpose") if k in stage_ms and stage_ms[k] > 0}
     out = {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -355,15 +357,55 @@ def run_llsa(args, ws, rank, local):
                    "flops_per_step": work["step_flops"], "flops_counted": "14*d per (query, key) pair: "
                    "fwd 4d, bwd 10d (S, dP, dV, dK, dQ); selection excluded"},
         "stage_ms": stage_ms,
+        "stage_gbs": stage_gbs,
         "roofline": roof,
         "e2e": {"value": round(ws * work["step_flops"] / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if rank == 0 and ws == 1 and not args.no_dense:
+        out["dense_sdpa"] = dense_comparator(w, dev, ms_step)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, x, s)
     return out
+
+
+def dense_comparator(w, dev, llsa_ms):
+    """Context, not a target: PyTorch's fused dense attention (scaled_dot_
+    product_attention, flash / cuDNN / memory-efficient backends only) forward
+    plus backward on the same shape and dtype, timed with CUDA events."""
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+    import torch.nn.functional as F
+    shape = (w.batch, w.heads, w.n, w.d)
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    g = torch.Generator(device=dev).manual_seed(11)
+    q, k, v = (torch.randn(shape, device=dev, dtype=td, generator=g).requires_grad_(True) for _ in range(3))
+    do = torch.randn(shape, device=dev, dtype=td, generator=g)
+    backends = [SDPBackend.FLASH_ATTENTION, SDPBackend.CUDNN_ATTENTION, SDPBackend.EFFICIENT_ATTENTION]
+    try:
+        with sdpa_kernel(backends):
+            def step():
+                o = F.scaled_dot_product_attention(q, k, v)
+                o.backward(do)
+            for _ in range(2):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 3
+            e0.record()
+            for _ in range(reps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+    except RuntimeError as err:  # no fused backend for this shape / device
+        return {"unavailable": str(err).splitlines()[0][:160]}
+    flops = 14 * w.d * w.batch * w.heads * w.n * w.n
+    return {"ms_per_step": round(ms, 3), "value": round(flops / (ms * 1e-3) / 1e12, 1), "unit": "TFLOP/s",
+            "flops_per_step": flops, "flops_counted": "14*d per (query, key) pair over all N^2 pairs",
+            "llsa_speedup": round(ms / llsa_ms, 2),
+            "what": "torch scaled_dot_product_attention fwd+bwd, dense, same shape and dtype, random inputs"}
 
 
 def llsa_tensor_kernels(records):
@@ -448,6 +490,7 @@ def main():
     ap.add_argument("--impl", choices=["llsa", "reference"], default="llsa")
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture of this build")
     args = ap.parse_args()

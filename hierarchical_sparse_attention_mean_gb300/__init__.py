@@ -25,6 +25,8 @@ _lib = None
 
 LLSA_DTYPE_BF16, LLSA_DTYPE_F32 = 0, 1
 LLSA_ENRICH_TOP1 = 0
+LLSA_ENRICH_ANCESTOR = 1
+_RULES = {"top1": LLSA_ENRICH_TOP1, "ancestor": LLSA_ENRICH_ANCESTOR}
 OP_POOL, OP_SELECT, OP_FWD, OP_TRANSPOSE, OP_BWD = range(5)
 MAX_LEVELS = 8
 
@@ -107,13 +109,17 @@ class Params:
     enrich_levels: int = -1    # -1: all levels; 0: no enrichment
     dtype: str = "bf16"        # "bf16" or "fp32"
     scale: float = 0.0         # 0: 1/sqrt(d)
+    enrich_rule: str = "top1"  # "top1" or "ancestor"
 
     def c(self) -> _Params:
         dt = {"bf16": LLSA_DTYPE_BF16, "fp32": LLSA_DTYPE_F32}.get(self.dtype)
         if dt is None:
             raise ValueError(f"dtype must be 'bf16' or 'fp32', not {self.dtype!r}")
+        rule = _RULES.get(self.enrich_rule)
+        if rule is None:
+            raise ValueError(f"enrich_rule must be 'top1' or 'ancestor', not {self.enrich_rule!r}")
         return _Params(self.batch, self.heads, self.n, self.d, self.block, self.levels, self.topk,
-                       self.enrich_levels, dt, self.scale, LLSA_ENRICH_TOP1)
+                       self.enrich_levels, dt, self.scale, rule)
 
     @staticmethod
     def like(q, **kw) -> "Params":

@@ -113,7 +113,7 @@ static int derive(const llsa_params* p, Shape* s) {
     if (!p) return LLSA_ERR_INVALID_ARG;
     if (p->batch < 0 || p->heads < 0 || p->n < 1 || p->topk < 1) return LLSA_ERR_INVALID_ARG;
     if (p->dtype != LLSA_DTYPE_BF16 && p->dtype != LLSA_DTYPE_F32) return LLSA_ERR_DTYPE;
-    if (p->enrich_rule != LLSA_ENRICH_TOP1) return LLSA_ERR_INVALID_ARG;
+    if (p->enrich_rule != LLSA_ENRICH_TOP1 && p->enrich_rule != LLSA_ENRICH_ANCESTOR) return LLSA_ERR_INVALID_ARG;
     if (!(p->scale >= 0.0f) || isinf(p->scale)) return LLSA_ERR_INVALID_ARG;
     if (p->d < 8 || p->d > 256 || p->d % 8 != 0) return LLSA_ERR_SHAPE;
     if (p->block < 2 || p->block > 1024) return LLSA_ERR_SHAPE;
@@ -151,7 +151,7 @@ static int derive(const llsa_params* p, Shape* s) {
     }
     s->level_idx_per_slice = lio;
     s->slices = (long long)p->batch * p->heads;
-    s->n = p->n; s->d = p->d; s->B = p->block; s->L = L; s->Le = Le;
+    s->n = p->n; s->d = p->d; s->B = p->block; s->L = L; s->Le = Le; s->rule = p->enrich_rule;
     s->K1 = s->topk_level[1]; s->T = s->n_level[1]; s->P = off; s->dtype = p->dtype;
     s->scale = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
     if (s->slices * (long long)p->n * p->d > (1LL << 40)) return LLSA_ERR_UNSUPPORTED;

@@ -21,6 +21,7 @@ struct AttnArgs {
     float scale, lnB;
     LevelTable lv;
     int* status;
+    int rule;  // enrichment rule
 };
 
 AttnArgs make_attn_args(const Shape& s);

@@ -417,8 +417,9 @@ void allow_smem(K kernel, size_t smem) {
 // query-block order, of the coarse partials of the query blocks that used it.
 // One warp per pooled row. Level-1 tokens are fine blocks their users also
 // selected (TOP1 picks from the selection), so the fine CSC column lists the
-// candidates; level l >= 2 tokens scan the level's ancestors (one rank-1 token
-// per ancestor, shared by its B^(l-1) query blocks). Candidates are tested 32
+// candidates (under ANCESTOR the level-1 token e is used by block e alone);
+// level l >= 2 tokens scan the level's ancestors (one token per ancestor,
+// shared by its B^(l-1) query blocks). Candidates are tested 32
 // at a time (one per lane), the hits compacted in lane order, and their rows
 // summed in that order with several rows in flight; each lane owns kCols
 // consecutive columns.
@@ -486,7 +487,10 @@ __global__ void __launch_bounds__(32 * kReduceWarps) coarse_reduce_kernel(AttnAr
         }
     };
     int* h = hits[warp];
-    if (l == 1) {
+    if (l == 1 && a.rule == LLSA_ENRICH_ANCESTOR) {
+        // the level-1 token e is block e's own pooled keys: used by block e only
+        add_rows(1, [&](int) { return e; });
+    } else if (l == 1) {
         const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
         const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
         const int beg = cp[e], end = cp[e + 1];
@@ -538,6 +542,7 @@ AttnArgs make_attn_args(const Shape& s) {
     a.lnB = logf((float)s.B);
     a.lv = level_table(s);
     a.status = status_ptr();
+    a.rule = s.rule;
     return a;
 }
 

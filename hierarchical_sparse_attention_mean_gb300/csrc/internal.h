@@ -18,6 +18,7 @@ struct Shape {
     int n, d, B, L, Le, K1, T, P;
     int dtype;
     float scale;
+    int rule;  // enrichment rule (LLSA_ENRICH_*)
     int n_level[LLSA_MAX_LEVELS + 1];
     int topk_level[LLSA_MAX_LEVELS + 1];
     int row_offset[LLSA_MAX_LEVELS + 1];

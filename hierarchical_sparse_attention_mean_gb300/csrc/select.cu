@@ -47,6 +47,7 @@ struct SelectArgs {
     int rows_per_cta;
     int C;                 // candidates per row
     int n_parent;          // rows of the parent level (index check)
+    int rule;              // enrichment rule
     int* status;
 };
 
@@ -171,8 +172,9 @@ __global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs 
         for (int k2 = 0; k2 < a.Kl; k2++) rank += krow[k2] < v;
         orow[rank] = v;
     }
-    // enrichment index: every level-1 descendant of this row gets its rank-1
-    const int top1 = krow[0];
+    // enrichment index: every level-1 descendant of this row gets the row's
+    // rank-1 selection (TOP1) or the row itself (ANCESTOR)
+    const int top1 = a.rule == LLSA_ENRICH_ANCESTOR ? row : krow[0];
     int* crow = a.coarse + (slice * a.T + (long long)row * a.span) * a.L + (a.level - 1);
     for (int q = lane; q < a.span; q += 32) crow[(long long)q * a.L] = top1;
 }
@@ -232,6 +234,7 @@ int launch_select(const Shape& s, const float* pyr, int32_t* sel_idx, int32_t* c
         a.level = l;
         a.span = (int)span;
         a.status = status_ptr();
+        a.rule = s.rule;
         if (l == s.L) {
             a.parent = nullptr;
             a.parent_stride = 0;

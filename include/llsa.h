@@ -56,10 +56,14 @@ enum {
 
 enum { LLSA_DTYPE_BF16 = 0, LLSA_DTYPE_F32 = 1 };
 
-/* Enrichment rule: which coarse token of level l joins query block i's keys.
+/* Enrichment rule: which coarse token of level l joins query block i's keys
+ * ("Core claim": one coarse token from every level; the page does not say
+ * which, so both readings are offered).
  * TOP1: the rank-1 selection of level l for i's level-l ancestor
- * floor(i / B^(l-1)) ("Core claim": one coarse token from every level). */
-enum { LLSA_ENRICH_TOP1 = 0 };
+ *       floor(i / B^(l-1));
+ * ANCESTOR: that ancestor itself, the level-l token whose B^l tokens contain
+ *       query block i. */
+enum { LLSA_ENRICH_TOP1 = 0, LLSA_ENRICH_ANCESTOR = 1 };
 
 enum { LLSA_OP_POOL = 0, LLSA_OP_SELECT = 1, LLSA_OP_FWD = 2, LLSA_OP_TRANSPOSE = 3, LLSA_OP_BWD = 4 };
 
@@ -73,7 +77,7 @@ typedef struct llsa_params {
     int enrich_levels;  /* L_e; -1 selects L; 0 disables enrichment */
     int dtype;          /* LLSA_DTYPE_BF16 or LLSA_DTYPE_F32 */
     float scale;        /* softmax scale; 0 selects 1/sqrt(d) */
-    int enrich_rule;    /* LLSA_ENRICH_TOP1 */
+    int enrich_rule;    /* LLSA_ENRICH_TOP1 or LLSA_ENRICH_ANCESTOR */
 } llsa_params;
 
 /* Sizes derived from the parameters. */

@@ -65,7 +65,7 @@ def _load():
                                      _i32p, _i32p, ctypes.POINTER(_ll)]
     lib.orc_pair_scores.argtypes = [_f64p, _f64p, ctypes.c_int, _i64p, _i64p, _ll, _f64p]
     lib.orc_select_all.argtypes = [_f64p, _f64p, _ll, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                   _i32p, _i32p, _i32p, ctypes.POINTER(_ll)]
+                                   ctypes.c_int, _i32p, _i32p, _i32p, ctypes.POINTER(_ll)]
     lib.orc_fwd.argtypes = [_f32p, _f32p, _f32p, _f64p, _f64p, _ll, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                             ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_double,
                             ctypes.c_void_p, _ll, _f64p, _f64p]
@@ -181,8 +181,13 @@ def pair_scores(qpyr_l, kpyr_l, rows, cols) -> np.ndarray:
     return out
 
 
-def select_all(qpyr, kpyr, n: int, B: int, L: int, K: int) -> dict:
-    """All levels coarsest-first plus the TOP1 enrichment index.
+RULES = {"top1": 0, "ancestor": 1}
+
+
+def select_all(qpyr, kpyr, n: int, B: int, L: int, K: int, rule: str = "top1") -> dict:
+    """All levels coarsest-first plus the enrichment index (rule "top1": the
+    rank-1 selection of the query block's level-l ancestor; "ancestor": that
+    ancestor itself).
     Returns {'levels': [None, I1, ..., IL], 'top1': [None, t1, ...],
              'coarse': int32 [n_1, L], 'work': scored pairs}."""
     qpyr, kpyr = _f64(qpyr), _f64(kpyr)
@@ -193,7 +198,8 @@ def select_all(qpyr, kpyr, n: int, B: int, L: int, K: int) -> dict:
     top1_all = np.empty(sum(sizes[1:]), np.int32)
     coarse = np.empty((sizes[1], L), np.int32)
     work = _ll(0)
-    _check(_load().orc_select_all(qpyr, kpyr, n, d, B, L, K, idx_all, top1_all, coarse, ctypes.byref(work)),
+    _check(_load().orc_select_all(qpyr, kpyr, n, d, B, L, K, RULES[rule], idx_all, top1_all, coarse,
+                                  ctypes.byref(work)),
            "select_all")
     levels, top1 = [None], [None]
     io, to = 0, 0
@@ -276,7 +282,7 @@ def bwd_dkv_blocks(q, k, v, kpyr, vpyr, o, lse, dout, B, L, Le, sel, coarse, sca
 # Whole path over [bh, n, d] arrays
 # --------------------------------------------------------------------------
 
-def run(q, k, v, dout=None, *, B=16, K=8, L=None, Le=None, scale=None, threads=1, backward=True):
+def run(q, k, v, dout=None, *, B=16, K=8, L=None, Le=None, scale=None, threads=1, backward=True, rule="top1"):
     """The whole hot path for every (batch, head) slice of q, k, v [bh, n, d]
     (any leading shape is flattened to bh). Returns a dict of per-slice lists
     plus stacked outputs 'o', 'lse', and, with dout, 'dq', 'dk', 'dv'."""
@@ -297,7 +303,7 @@ def run(q, k, v, dout=None, *, B=16, K=8, L=None, Le=None, scale=None, threads=1
 
     def one(s):
         qp, kp, vp = pool(q3[s], B, L), pool(k3[s], B, L), pool(v3[s], B, L)
-        sel = select_all(qp, kp, n, B, L, K)
+        sel = select_all(qp, kp, n, B, L, K, rule)
         I1, coarse = sel["levels"][1], sel["coarse"]
         o, lse = fwd(q3[s], k3[s], v3[s], kp, vp, B, L, Le, I1, coarse, scale)
         col_ptr, row_idx = transpose(I1, T)

@@ -26,7 +26,8 @@
  *     stored index rows are sorted ascending.
  *   - K at a level is clamped to the number of candidates there.
  *   - Enrichment token of level l for query block i: the rank-1 selection of
- *     level l for i's level-l ancestor (TOP1 rule).
+ *     level l for i's level-l ancestor (TOP1 rule, the default), or that
+ *     ancestor itself (ANCESTOR rule).
  *   - Reweighting adds ln(B^l) to the coarse token's logit; softmax scale is
  *     1/sqrt(d) unless the caller gives one.
  *
@@ -211,19 +212,22 @@ int orc_pair_scores(const double *qpyr_l, const double *kpyr_l, int d,
 
 /* All levels, coarsest first, plus the enrichment index.
  *   qpyr, kpyr : pyramids (levels 1..L one after another).
+ *   rule       : 0 (TOP1) or 1 (ANCESTOR), see coarse.
  *   idx_all    : level 1 first: n_1*K_1 ints, then n_2*K_2, ... n_L*K_L.
  *   top1_all   : n_1 + ... + n_L rank-1 indices, level 1 first.
  *   coarse     : n_1 rows of L entries; coarse[i*L + (l-1)] is the level-l
- *                enrichment token of query block i: the rank-1 selection of
- *                level l for i's ancestor floor(i / B^(l-1)).
+ *                enrichment token of query block i: for TOP1 the rank-1
+ *                selection of level l for i's ancestor floor(i / B^(l-1)),
+ *                for ANCESTOR that ancestor itself.
  *   work_out   : number of scored candidate pairs over all levels. */
-int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, int B, int L, int K,
+int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, int B, int L, int K, int rule,
                    int *idx_all, int *top1_all, int *coarse, long long *work_out)
 {
     long long nl[64];
     int kl[64];
     if (L < 1 || L > 60 || orc_level_sizes(n, B, L, nl) != ORC_OK) return ORC_ERR_ARG;
     if (orc_level_topk(n, B, L, K, kl) != ORC_OK) return ORC_ERR_ARG;
+    if (rule != 0 && rule != 1) return ORC_ERR_ARG;
     long long row_off[64], idx_off[64], t1_off[64];
     row_off[1] = 0; idx_off[1] = 0; t1_off[1] = 0;
     for (int l = 2; l <= L; l++) {
@@ -241,7 +245,8 @@ int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, i
     }
     long long span = 1;
     for (int l = 1; l <= L; l++) {
-        for (long long i = 0; i < nl[1]; i++) coarse[i * L + (l - 1)] = top1_all[t1_off[l] + i / span];
+        for (long long i = 0; i < nl[1]; i++)
+            coarse[i * L + (l - 1)] = rule == 1 ? (int)(i / span) : top1_all[t1_off[l] + i / span];
         span *= B;
     }
     return ORC_OK;

@@ -82,6 +82,17 @@ def test_invalid_parameters_rejected_on_host(lib, kw, code):
     assert e.value.code == code
 
 
+def test_enrichment_rules(lib):
+    for rule in ("top1", "ancestor"):
+        assert llsa.get_sizes(llsa.Params(1, 1, 4096, 64, enrich_rule=rule)).keys_per_query == 8 * 16 + 2
+    p = llsa.Params(1, 1, 4096, 64).c()
+    p.enrich_rule = 2  # no such rule
+    s = llsa._Sizes()
+    assert lib.llsa_get_sizes(ctypes.byref(p), ctypes.byref(s)) == -1
+    with pytest.raises(ValueError):
+        llsa.Params(1, 1, 4096, 64, enrich_rule="allk").c()
+
+
 def test_bad_dtype_and_empty_input(lib):
     p = llsa.Params(1, 1, 4096, 64).c()
     p.dtype = 7

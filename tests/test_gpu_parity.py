@@ -273,3 +273,19 @@ def test_fine_logits_far_above_pooled_logits():
     assert_lse(out["lse"], ref["lse"])
     for key in ("dq", "dk", "dv"):
         assert_close(key, out[key], ref[key], "bf16")
+
+
+@pytest.mark.parametrize("name", ["n4096-bf16", "B4-L4-fp32", "d128-K16"])
+def test_ancestor_rule_end_to_end(name):
+    """ANCESTOR enrichment: selection identical to TOP1's, the enrichment index
+    is each block's own ancestor, outputs and gradients match the oracle."""
+    w = CASES[name]
+    x = synth.make_inputs(w)
+    ref = run_oracle(w, x, rule="ancestor")
+    out, _ = gpu_stage_outputs(w, x, p=params_of(w, enrich_rule="ancestor"), backward=w.backward)
+    T, L = w.n // w.block, ref["L"]
+    for s in range(w.bh):
+        for l in range(1, L + 1):
+            np.testing.assert_array_equal(out["gpu_coarse"][s][:, l - 1], np.arange(T) // w.block ** (l - 1))
+    excluded = compare_end_to_end(w, ref, out)
+    assert excluded <= max(1, 0.01 * w.bh * (w.n // w.block))

@@ -463,3 +463,58 @@ def test_generator_moments_and_bf16():
     r = synth.bf16_round(np.array([1.0, 1.00390625, 1.01171875, -3.1415926], np.float32))
     assert r[0] == 1.0 and r[1] == 1.0 and r[2] == 1.015625   # ties to even
     assert (r.view(np.uint32) & 0xFFFF).max() == 0
+
+
+# ---------------------------------------------------- ANCESTOR enrichment ---
+
+def test_ancestor_rule_index_and_selection():
+    """ANCESTOR: the level-l token of query block i is i's own level-l
+    ancestor floor(i / B^(l-1)); the Top-K selection does not change."""
+    n, B, K, d = 4096, 16, 4, 8
+    x = rng_inputs(n, d, seed=91)
+    L = oracle.num_levels(n, B)
+    a = oracle.run(x["q"], x["k"], x["v"], B=B, K=K, backward=False, rule="ancestor")["slices"][0]["sel"]
+    t = oracle.run(x["q"], x["k"], x["v"], B=B, K=K, backward=False)["slices"][0]["sel"]
+    T = n // B
+    for l in range(1, L + 1):
+        np.testing.assert_array_equal(a["coarse"][:, l - 1], np.arange(T) // B ** (l - 1))
+        np.testing.assert_array_equal(a["levels"][l], t["levels"][l])
+
+
+@pytest.mark.parametrize("n,B,K,Le", [(1024, 16, 4, None), (512, 2, 3, 3)])
+def test_ancestor_rule_equals_dense_mask(n, B, K, Le):
+    d = 8
+    x = rng_inputs(n, d, seed=93)
+    L = oracle.num_levels(n, B)
+    Le = L if Le is None else Le
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=K, Le=Le, rule="ancestor")
+    s = res["slices"][0]
+    o_ref, lse_ref, _ = dense_masked(x["q"][0], x["k"][0], x["v"][0], B, L, Le,
+                                     s["sel"]["levels"][1], s["sel"]["coarse"], res["scale"])
+    np.testing.assert_allclose(s["o"], o_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(s["lse"], lse_ref, rtol=1e-12, atol=1e-12)
+    gq, gk, gv = _torch_masked_grads(x, B, L, Le, s["sel"]["levels"][1], s["sel"]["coarse"], res["scale"])
+    np.testing.assert_allclose(s["dq"], gq, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s["dk"], gk, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s["dv"], gv, rtol=1e-9, atol=1e-11)
+
+
+def test_ancestor_full_selection_closed_form():
+    """K*B >= N with L = 1 under ANCESTOR: dense attention over all tokens plus,
+    for query block i, the mean of block i's own keys and values with logit
+    bias ln B (closed form, torch, fp64)."""
+    n, B, d = 1024, 16, 16
+    x = rng_inputs(n, d, seed=95)
+    scale = 1.0 / math.sqrt(d)
+    res = oracle.run(x["q"], x["k"], x["v"], B=B, K=64, backward=False, rule="ancestor")
+    assert res["L"] == 1
+    q, k, v = (torch.tensor(x[a][0], dtype=torch.float64) for a in ("q", "k", "v"))
+    kc = k.reshape(-1, B, d).mean(1)                    # block i's own pooled key
+    vc = v.reshape(-1, B, d).mean(1)
+    lc = scale * (q.reshape(-1, B, d) * kc[:, None, :]).sum(-1).reshape(n, 1) + math.log(B)
+    z = torch.cat([scale * q @ k.T, lc], 1)
+    lse = torch.logsumexp(z, 1)
+    p = torch.exp(z - lse[:, None])
+    o = p[:, :n] @ v + p[:, n:] * vc.repeat_interleave(B, 0)
+    np.testing.assert_allclose(res["slices"][0]["o"], o.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(res["slices"][0]["lse"], lse.numpy(), rtol=1e-12, atol=1e-12)
