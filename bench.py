@@ -364,11 +364,40 @@ def run_llsa(args, ws, rank, local):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if rank == 0 and ws == 1:
+        out["reorder"] = reorder_rate(w, dev, peaks)
     if rank == 0 and ws == 1 and not args.no_dense:
         out["dense_sdpa"] = dense_comparator(w, dev, ms_step)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, x, s)
     return out
+
+
+def reorder_rate(w, dev, peaks):
+    """Index reordering (hierarchical tile order) of one token tensor of the
+    workload's shape, outside the step: HBM GB/s of `llsa_reorder`."""
+    from hierarchical_sparse_attention_mean_gb300 import llsa_reorder, Params
+    side, s = int(round(math.sqrt(w.n))), int(round(math.sqrt(w.block)))
+    if side * side != w.n or s * s != w.block:
+        return {"unavailable": "the workload is not a square image with B = s^2"}
+    td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    p = Params(w.batch, w.heads, w.n, w.d, block=w.block, topk=w.topk, dtype=w.dtype)
+    x = torch.randn(w.batch, w.heads, w.n, w.d, device=dev, dtype=td)
+    y = torch.empty_like(x)
+    for _ in range(3):
+        llsa_reorder(p, side, side, x, y)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 20
+    e0.record()
+    for i in range(reps):
+        llsa_reorder(p, side, side, x, y, inverse=bool(i & 1))
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 2 * x.numel() * x.element_size()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": round(ms, 4), "bytes": nbytes, "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 3),
+            "what": "one [batch, heads, N, d] tensor to the tile order and back, alternating, 20 launches"}
 
 
 def dense_comparator(w, dev, llsa_ms):

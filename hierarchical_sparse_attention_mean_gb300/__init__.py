@@ -76,6 +76,7 @@ def _load():
     lib.llsa_select.argtypes = [P, vp, vp, vp, vp, vp, sz, vp]
     lib.llsa_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.llsa_index_transpose.argtypes = [P, vp, vp, vp, vp, sz, vp]
+    lib.llsa_reorder.argtypes = [P, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int, vp]
     lib.llsa_bwd.argtypes = [P] + [vp] * 14 + [vp, sz, vp]
     lib.llsa_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.llsa_strerror.argtypes = [ctypes.c_int]
@@ -227,6 +228,14 @@ def llsa_index_transpose(p: Params, sel_idx, col_ptr, row_idx, ws, stream=None):
     _check(_load().llsa_index_transpose(ctypes.byref(p.c()), _ptr(sel_idx, "sel_idx", torch.int32),
                                         _ptr(col_ptr, "col_ptr", torch.int32), _ptr(row_idx, "row_idx", torch.int32),
                                         w, wb, _stream(stream)), "llsa_index_transpose")
+
+
+def llsa_reorder(p: Params, height: int, width: int, x, out, inverse: bool = False, stream=None):
+    """Hierarchical tile order of the N = height * width tokens of x
+    [batch, heads, N, d] into out (inverse=True maps back to raster order)."""
+    td = _tok_dtype(p)
+    _check(_load().llsa_reorder(ctypes.byref(p.c()), int(height), int(width), _ptr(x, "x", td), _ptr(out, "out", td),
+                                1 if inverse else 0, _stream(stream)), "llsa_reorder")
 
 
 def llsa_bwd(p: Params, q, k, v, o, lse, dout, pyr, sel_idx, coarse_idx, col_ptr, row_idx, dq, dk, dv, ws,

@@ -219,6 +219,26 @@ int llsa_pool(const llsa_params* p, const void* q, const void* k, const void* v,
     return launch_pool(s, q, k, v, pyr, static_cast<cudaStream_t>(stream));
 }
 
+int llsa_reorder(const llsa_params* p, int height, int width, const void* in, void* out, int inverse, void* stream) {
+    Shape s;
+    LLSA_TRY(derive(p, &s));
+    if (inverse != 0 && inverse != 1) return LLSA_ERR_INVALID_ARG;
+    int root = 2;
+    while (root * root < s.B) root++;
+    if (root * root != s.B) return LLSA_ERR_SHAPE;
+    if (height != width || height < 1 || (long long)height * width != s.n) return LLSA_ERR_SHAPE;
+    int digits = 0;
+    for (int side = height; side > 1; side /= root) {
+        if (side % root != 0) return LLSA_ERR_SHAPE;
+        digits++;
+    }
+    if (s.slices == 0) return LLSA_OK;
+    LLSA_TRY(check_ptrs({in, out}));
+    if (in == out) return LLSA_ERR_INVALID_ARG;
+    LLSA_TRY(check_device());
+    return launch_reorder(s, width, root, digits, in, out, inverse, static_cast<cudaStream_t>(stream));
+}
+
 int llsa_select(const llsa_params* p, const float* pyr, int32_t* sel_idx, int32_t* coarse_idx,
                 int32_t* level_idx, void* ws, size_t ws_bytes, void* stream) {
     (void)ws; (void)ws_bytes;

@@ -79,6 +79,8 @@ int launch_select(const Shape& s, const float* pyr, int32_t* sel_idx, int32_t* c
                   cudaStream_t st);
 int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, const float* pyr,
                const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, cudaStream_t st);
+int launch_reorder(const Shape& s, int side, int root, int digits, const void* in, void* out, int inverse,
+                   cudaStream_t st);
 int launch_transpose(const Shape& s, const int32_t* sel, int rows, int K, int ncols, int32_t* col_ptr,
                      int32_t* row_idx, int32_t* scratch, cudaStream_t st);
 size_t bwd_workspace_bytes(const Shape& s);

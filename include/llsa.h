@@ -192,6 +192,20 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
 int llsa_index_transpose_noalloc(const llsa_params *p, const int32_t *sel_idx, int32_t *col_ptr, int32_t *row_idx,
                                  void *stream);
 
+/* Hierarchical tile order of the tokens of a square image (referee comments
+ * on Sec. 5.1 and Figure 2, index reordering; the page gives no formula, the
+ * reading is: with B = s^2 and an s^m x s^m raster image, every run of B^l
+ * consecutive positions of the new order is an s^l x s^l square of pixels,
+ * applied recursively; pixel (r, c) with base-s digits r_k, c_k goes to
+ * position sum_k (r_k * s + c_k) * B^k).
+ *   in, out  : [batch, heads, N, d] in p->dtype, distinct buffers (16-byte
+ *              aligned); out receives in's rows in the new order (inverse = 0,
+ *              raster -> tile order) or back (inverse = 1).
+ *   height, width : the image, height * width == N, height == width == s^m.
+ * Errors: LLSA_ERR_SHAPE unless B is a perfect square s^2 (s >= 2) and the
+ * image is s^m x s^m; LLSA_ERR_INVALID_ARG for inverse not 0 / 1 or in == out. */
+int llsa_reorder(const llsa_params *p, int height, int width, const void *in, void *out, int inverse, void *stream);
+
 /* Reads (after synchronising `stream`) and clears the device status word of
  * the current device: LLSA_OK, LLSA_ERR_TIMEOUT or LLSA_ERR_BAD_INDEX. */
 int llsa_get_status(void *stream, int *device_status);

@@ -325,3 +325,29 @@ def run(q, k, v, dout=None, *, B=16, K=8, L=None, Le=None, scale=None, threads=1
         for key in ("dq", "dk", "dv"):
             out[key] = np.stack([r[key] for r in per])
     return out
+
+
+def tile_order(height: int, width: int, B: int) -> np.ndarray:
+    """Hierarchical tile order of an s^m x s^m raster image, B = s^2 (reading of
+    the page's index reordering, referee comments on Sec. 5.1 / Figure 2):
+    pixel (r, c) with base-s digits r_k, c_k goes to position
+    sum_k (r_k * s + c_k) * B^k, so every run of B^l consecutive positions is
+    an s^l x s^l square. Returns src with src[p] = the raster token at
+    position p (the forward permutation reads in[src[p]] into out[p])."""
+    s = int(round(math.sqrt(B)))
+    if s * s != B or s < 2 or height != width:
+        raise ValueError("need B = s^2 and a square image")
+    m, side = 0, height
+    while side > 1:
+        if side % s:
+            raise ValueError("side must be a power of sqrt(B)")
+        side //= s
+        m += 1
+    r, c = np.divmod(np.arange(height * width, dtype=np.int64), width)
+    pos = np.zeros(height * width, np.int64)
+    for k in range(m):
+        rk, ck = (r // s ** k) % s, (c // s ** k) % s
+        pos += (rk * s + ck) * B ** k
+    src = np.empty_like(pos)
+    src[pos] = np.arange(height * width)
+    return src

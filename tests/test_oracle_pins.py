@@ -518,3 +518,38 @@ def test_ancestor_full_selection_closed_form():
     o = p[:, :n] @ v + p[:, n:] * vc.repeat_interleave(B, 0)
     np.testing.assert_allclose(res["slices"][0]["o"], o.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(res["slices"][0]["lse"], lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------- index reordering ---
+
+def test_tile_order_worked_example():
+    """8x8 image, B = 4 (s = 2): the first 4 positions are the 2x2 square at
+    the origin, row by row; positions 4..7 the next 2x2 square to the right;
+    positions 0..15 the 4x4 square at the origin."""
+    src = oracle.tile_order(8, 8, 4)
+    assert src[:4].tolist() == [0, 1, 8, 9]
+    assert src[4:8].tolist() == [2, 3, 10, 11]
+    assert sorted(src[:16].tolist()) == sorted(r * 8 + c for r in range(4) for c in range(4))
+
+
+@pytest.mark.parametrize("side,B", [(64, 16), (256, 16), (32, 4), (27, 9)])
+def test_tile_order_runs_are_squares(side, B):
+    src = oracle.tile_order(side, side, B)
+    n = side * side
+    assert np.array_equal(np.sort(src), np.arange(n))              # a permutation
+    s = int(round(math.sqrt(B)))
+    run = B
+    while run <= n:
+        r, c = np.divmod(src.reshape(-1, run), side)
+        w = int(round(math.sqrt(run)))
+        assert (r.max(1) - r.min(1) == w - 1).all() and (c.max(1) - c.min(1) == w - 1).all()
+        assert (r.min(1) % w == 0).all() and (c.min(1) % w == 0).all()
+        run *= B
+    assert s ** 2 == B
+
+
+def test_tile_order_rejects_non_square_blocks():
+    with pytest.raises(ValueError):
+        oracle.tile_order(64, 64, 8)
+    with pytest.raises(ValueError):
+        oracle.tile_order(48, 48, 16)
