@@ -366,11 +366,30 @@ def run_llsa(args, ws, rank, local):
     }
     if rank == 0 and ws == 1:
         out["reorder"] = reorder_rate(w, dev, peaks)
+        out["routing_recall"] = routing_recall(p, b, w, dev)
     if rank == 0 and ws == 1 and not args.no_dense:
         out["dense_sdpa"] = dense_comparator(w, dev, ms_step)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, x, s)
     return out
+
+
+def routing_recall(p, b, w, dev):
+    """Share of the exhaustive level-1 Top-K (single-level full scoring of the
+    level-1 tokens) that the hierarchical selection of the timed step keeps,
+    over every query block of every slice, with the exhaustive kernel's time."""
+    import hierarchical_sparse_attention_mean_gb300 as llsa
+    T = llsa.get_sizes(p).n_blocks
+    ex = torch.empty(w.bh, T, min(w.topk, T), dtype=torch.int32, device=dev)
+    llsa.llsa_select_exhaustive(p, b.pyr, ex)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    llsa.llsa_select_exhaustive(p, b.pyr, ex)
+    e1.record()
+    torch.cuda.synchronize()
+    return {"value": round(llsa.routing_recall(b.sel_idx, ex), 4), "exhaustive_ms": round(e0.elapsed_time(e1), 3),
+            "what": "fraction of the exhaustive level-1 Top-K held by the hierarchical selection, all query blocks"}
 
 
 def reorder_rate(w, dev, peaks):

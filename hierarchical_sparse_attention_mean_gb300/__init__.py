@@ -77,6 +77,7 @@ def _load():
     lib.llsa_fwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.llsa_index_transpose.argtypes = [P, vp, vp, vp, vp, sz, vp]
     lib.llsa_reorder.argtypes = [P, ctypes.c_int, ctypes.c_int, vp, vp, ctypes.c_int, vp]
+    lib.llsa_select_exhaustive.argtypes = [P, vp, vp, vp]
     lib.llsa_bwd.argtypes = [P] + [vp] * 14 + [vp, sz, vp]
     lib.llsa_get_status.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     lib.llsa_strerror.argtypes = [ctypes.c_int]
@@ -228,6 +229,24 @@ def llsa_index_transpose(p: Params, sel_idx, col_ptr, row_idx, ws, stream=None):
     _check(_load().llsa_index_transpose(ctypes.byref(p.c()), _ptr(sel_idx, "sel_idx", torch.int32),
                                         _ptr(col_ptr, "col_ptr", torch.int32), _ptr(row_idx, "row_idx", torch.int32),
                                         w, wb, _stream(stream)), "llsa_index_transpose")
+
+
+def llsa_select_exhaustive(p: Params, pyr, sel_idx, stream=None):
+    """Exhaustive level-1 Top-K: sel_idx int32 [batch*heads, T, min(K, T)]."""
+    import torch
+    _check(_load().llsa_select_exhaustive(ctypes.byref(p.c()), _ptr(pyr, "pyr", torch.float32),
+                                          _ptr(sel_idx, "sel_idx", torch.int32), _stream(stream)),
+           "llsa_select_exhaustive")
+
+
+def routing_recall(hier_sel, exhaustive_sel) -> float:
+    """Share of the exhaustive level-1 Top-K entries that the hierarchical
+    selection also holds, over all rows (both int32 [.., T, K] tensors)."""
+    import torch
+    h = hier_sel.reshape(-1, hier_sel.shape[-1]).long()
+    e = exhaustive_sel.reshape(-1, exhaustive_sel.shape[-1]).long()
+    hit = (e[:, :, None] == h[:, None, :]).any(-1)
+    return float(hit.double().mean())
 
 
 def llsa_reorder(p: Params, height: int, width: int, x, out, inverse: bool = False, stream=None):

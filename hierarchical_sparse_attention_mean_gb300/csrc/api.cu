@@ -151,7 +151,7 @@ static int derive(const llsa_params* p, Shape* s) {
     }
     s->level_idx_per_slice = lio;
     s->slices = (long long)p->batch * p->heads;
-    s->n = p->n; s->d = p->d; s->B = p->block; s->L = L; s->Le = Le; s->rule = p->enrich_rule;
+    s->n = p->n; s->d = p->d; s->B = p->block; s->L = L; s->Le = Le; s->rule = p->enrich_rule; s->topk = p->topk;
     s->K1 = s->topk_level[1]; s->T = s->n_level[1]; s->P = off; s->dtype = p->dtype;
     s->scale = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
     if (s->slices * (long long)p->n * p->d > (1LL << 40)) return LLSA_ERR_UNSUPPORTED;
@@ -217,6 +217,15 @@ int llsa_pool(const llsa_params* p, const void* q, const void* k, const void* v,
     LLSA_TRY(check_ptrs({q, k, v, pyr}));
     LLSA_TRY(check_device());
     return launch_pool(s, q, k, v, pyr, static_cast<cudaStream_t>(stream));
+}
+
+int llsa_select_exhaustive(const llsa_params* p, const float* pyr, int32_t* sel_idx, void* stream) {
+    Shape s;
+    LLSA_TRY(derive(p, &s));
+    if (s.slices == 0) return LLSA_OK;
+    LLSA_TRY(check_ptrs({pyr, sel_idx}));
+    LLSA_TRY(check_device());
+    return launch_select_exhaustive(s, pyr, sel_idx, static_cast<cudaStream_t>(stream));
 }
 
 int llsa_reorder(const llsa_params* p, int height, int width, const void* in, void* out, int inverse, void* stream) {

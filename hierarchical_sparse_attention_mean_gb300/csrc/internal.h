@@ -19,6 +19,7 @@ struct Shape {
     int dtype;
     float scale;
     int rule;  // enrichment rule (LLSA_ENRICH_*)
+    int topk;  // K as requested (before the per-level clamp)
     int n_level[LLSA_MAX_LEVELS + 1];
     int topk_level[LLSA_MAX_LEVELS + 1];
     int row_offset[LLSA_MAX_LEVELS + 1];
@@ -79,6 +80,7 @@ int launch_select(const Shape& s, const float* pyr, int32_t* sel_idx, int32_t* c
                   cudaStream_t st);
 int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, const float* pyr,
                const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, cudaStream_t st);
+int launch_select_exhaustive(const Shape& s, const float* pyr, int32_t* out, cudaStream_t st);
 int launch_reorder(const Shape& s, int side, int root, int digits, const void* in, void* out, int inverse,
                    cudaStream_t st);
 int launch_transpose(const Shape& s, const int32_t* sel, int rows, int K, int ncols, int32_t* col_ptr,

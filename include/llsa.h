@@ -192,6 +192,16 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
 int llsa_index_transpose_noalloc(const llsa_params *p, const int32_t *sel_idx, int32_t *col_ptr, int32_t *row_idx,
                                  void *stream);
 
+/* Exhaustive single-level selection, the reference for routing recall (the
+ * referee's question of how much of the full fine-level Top-K the hierarchy
+ * keeps): every level-1 query token scores all T level-1 key tokens with the
+ * selection's score (raw pooled dot product, fp32) and keeps its
+ * K_x = min(K, T) best; ties go to the lower index.
+ *   pyr     : input from llsa_pool.
+ *   sel_idx : output int32 [batch*heads][T][K_x], rows ascending.
+ * Limits: K_x <= 64; d <= 256. */
+int llsa_select_exhaustive(const llsa_params *p, const float *pyr, int32_t *sel_idx, void *stream);
+
 /* Hierarchical tile order of the tokens of a square image (referee comments
  * on Sec. 5.1 and Figure 2, index reordering; the page gives no formula, the
  * reading is: with B = s^2 and an s^m x s^m raster image, every run of B^l

@@ -351,3 +351,21 @@ def tile_order(height: int, width: int, B: int) -> np.ndarray:
     src = np.empty_like(pos)
     src[pos] = np.arange(height * width)
     return src
+
+
+def select_exhaustive(qpyr, kpyr, n: int, B: int, L: int, K: int) -> np.ndarray:
+    """Single-level full scoring of the level-1 tokens (the reference of
+    routing recall): every level-1 query token keeps its min(K, T) best of all
+    T level-1 key tokens by the selection's score; ties to the lower index;
+    rows ascending. This is the coarsest level's rule applied to level 1."""
+    off, nl = level_rows(n, B, L)[1]
+    sel, _, _ = select_level(np.asarray(qpyr)[off:off + nl], np.asarray(kpyr)[off:off + nl], B, None, K)
+    return sel
+
+
+def routing_recall(hier_sel, exhaustive_sel) -> float:
+    """Share of the exhaustive level-1 Top-K entries that the hierarchical
+    level-1 selection also holds (rows aligned, [T, K] each)."""
+    h, e = np.asarray(hier_sel), np.asarray(exhaustive_sel)
+    hits = sum(len(set(e[i].tolist()) & set(h[i].tolist())) for i in range(e.shape[0]))
+    return hits / e.size

@@ -553,3 +553,35 @@ def test_tile_order_rejects_non_square_blocks():
         oracle.tile_order(64, 64, 8)
     with pytest.raises(ValueError):
         oracle.tile_order(48, 48, 16)
+
+
+# ---------------------------------------------------------- routing recall ---
+
+def test_exhaustive_selection_is_brute_force_top_k():
+    n, B, K, d = 4096, 16, 5, 8
+    x = rng_inputs(n, d, seed=101)
+    L = oracle.num_levels(n, B)
+    qp, kp = oracle.pool(x["q"][0], B, L), oracle.pool(x["k"][0], B, L)
+    ex = oracle.select_exhaustive(qp, kp, n, B, L, K)
+    T = n // B
+    s = (qp[:T].astype(np.float64) @ kp[:T].astype(np.float64).T)
+    for i in range(T):
+        order = np.lexsort((np.arange(T), -s[i]))      # score descending, index ascending
+        assert ex[i].tolist() == sorted(order[:K].tolist())
+
+
+def test_recall_is_one_when_the_hierarchy_sees_every_candidate():
+    """K*B >= n_2: the level-1 candidates are all T tokens, so the hierarchical
+    level-1 selection is the exhaustive one."""
+    n, B, d = 4096, 16, 8
+    x = rng_inputs(n, d, seed=103)
+    L = oracle.num_levels(n, B)
+    K = 16                                              # = n_2: full selection at level 2
+    qp, kp = oracle.pool(x["q"][0], B, L), oracle.pool(x["k"][0], B, L)
+    hier = oracle.select_all(qp, kp, n, B, L, K)["levels"][1]
+    ex = oracle.select_exhaustive(qp, kp, n, B, L, K)
+    assert oracle.routing_recall(hier, ex) == 1.0
+    K2 = 2                                              # sparse: recall strictly below 1 here
+    hier2 = oracle.select_all(qp, kp, n, B, L, K2)["levels"][1]
+    ex2 = oracle.select_exhaustive(qp, kp, n, B, L, K2)
+    assert 0.0 < oracle.routing_recall(hier2, ex2) < 1.0
