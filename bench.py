@@ -82,6 +82,28 @@ def recorded_traffic(workload: str, kernel: str):
     return table.get(kernel)
 
 
+def rank_workload(w0, rank: int):
+    """Each rank's problem: the same size, its own seed (weak scaling, no
+    data shared between ranks)."""
+    return synth.Workload(**{**w0.__dict__, "seed": w0.seed + 7919 * rank})
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """MAX of a per-rank time over all ranks (the job ends with its slowest
+    rank); the identity on one rank."""
+    if ws == 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(ws: int, flops_per_rank_step: float, ms_per_step: float) -> float:
+    """Whole-job throughput (TFLOP/s): every rank's work over the slowest
+    rank's time."""
+    return ws * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -212,7 +234,7 @@ def run_llsa(args, ws, rank, local):
     build.build()
     w0 = synth.WORKLOADS[args.workload]
     # each rank: an independent problem of the same size (weak scaling)
-    w = synth.Workload(**{**w0.__dict__, "seed": w0.seed + 7919 * rank})
+    w = rank_workload(w0, rank)
     x = synth.make_inputs(w, threads=os.cpu_count() or 8)
     shape = (w.batch, w.heads, w.n, w.d)
     td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
@@ -257,11 +279,7 @@ def run_llsa(args, ws, rank, local):
     launches = llsa.llsa_launch_count() - launches0
     llsa.profile_enable(False)
     records = llsa.profile_read(cap=64 * args.steps + 64)
-    elapsed = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([elapsed], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     ms_step = elapsed / args.steps
 
     # per-kernel durations from the events recorded around each launch
@@ -333,16 +351,12 @@ def run_llsa(args, ws, rank, local):
     s_up.wait_stream(stream)
     e3.record(s_up)
     torch.cuda.synchronize()
-    e2e_ms = e2.elapsed_time(e3) / e2e_steps
-    if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3) / e2e_steps, ws, dev)
     status = llsa.llsa_get_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    value = ws * work["step_flops"] / (ms_step * 1e-3) / 1e12
+    value = job_value(ws, work["step_flops"], ms_step)
     stage_gbs = {k: round(work["kernels"][k][0] / (stage_ms[k] * 1e-3) / 1e9, 1)
                  for k in ("pool_chunk", "transpose") if k in stage_ms and stage_ms[k] > 0}
     out = {
@@ -359,7 +373,7 @@ def run_llsa(args, ws, rank, local):
         "stage_ms": stage_ms,
         "stage_gbs": stage_gbs,
         "roofline": roof,
-        "e2e": {"value": round(ws * work["step_flops"] / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(job_value(ws, work["step_flops"], e2e_ms), 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clocks,
