@@ -419,7 +419,8 @@ void allow_smem(K kernel, size_t smem) {
 // selected (TOP1 picks from the selection), so the fine CSC column lists the
 // candidates (under ANCESTOR the level-1 token e is used by block e alone);
 // level l >= 2 tokens scan the level's ancestors (one token per ancestor,
-// shared by its B^(l-1) query blocks). Candidates are tested 32
+// shared by its B^(l-1) query blocks) and add each hit ancestor's span sum,
+// which coarse_span_kernel left in the row of its first block. Candidates are tested 32
 // at a time (one per lane), the hits compacted in lane order, and their rows
 // summed in that order with several rows in flight; each lane owns kCols
 // consecutive columns.
@@ -445,8 +446,8 @@ __device__ __forceinline__ void load_cols(const float* p, bool ok, float (&v)[kC
 }
 
 template <int kCols>  // columns per lane: d <= 32 * kCols, d % kCols == 0
-__global__ void __launch_bounds__(32 * kReduceWarps) coarse_reduce_kernel(AttnArgs a, int rows) {
-    constexpr int kUnroll = kCols >= 8 ? 2 : 16 / kCols;  // rows in flight
+__global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(AttnArgs a, int rows) {
+    constexpr int kUnroll = kCols >= 4 ? 2 : 4;  // rows in flight (spans are pre-summed: few rows per token)
     __shared__ int hits[kReduceWarps][32];
     const long long slice = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -514,11 +515,8 @@ __global__ void __launch_bounds__(32 * kReduceWarps) coarse_reduce_kernel(AttnAr
             const unsigned bits = __ballot_sync(0xffffffffu, hit);
             if (hit) h[__popc(bits & ((1u << lane) - 1u))] = anc;
             __syncwarp();
-            const int cnt = __popc(bits);
-            for (int j = 0; j < cnt; j++) {
-                const int first = h[j] * span;
-                add_rows(span, [&](int r) { return first + r; });
-            }
+            // ancestor anc's span sum sits in the row of block anc * span
+            add_rows(__popc(bits), [&](int r) { return h[r] * span; });
             __syncwarp();
         }
     }
@@ -528,6 +526,54 @@ __global__ void __launch_bounds__(32 * kReduceWarps) coarse_reduce_kernel(AttnAr
         for (int c = 0; c < kCols; c++) {
             a.dKc[out + c] = ak[c];
             a.dVc[out + c] = av[c];
+        }
+    }
+}
+
+// Pooled levels l >= 2: the query blocks under one level-l ancestor share its
+// token, so their partials are first summed per ancestor. Step `step` folds,
+// for every level l > step, each group of B consecutive rows at stride
+// B^(step-1) into the group's first row, in place and in ascending order;
+// after steps 1..l-1 the row of block anc * B^(l-1) holds ancestor anc's sum.
+template <int kCols>
+__global__ void __launch_bounds__(32 * kReduceWarps) coarse_span_kernel(AttnArgs a, int step, int stride, int groups) {
+    const long long slice = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int id = (int)(blockIdx.x * kReduceWarps + (threadIdx.x >> 5));
+    if (id >= (a.Le - step) * groups) return;
+    const int l = step + 1 + id / groups, grp = id % groups;
+    const int d = a.d;
+    const bool active = lane * kCols < d;
+    const long long rstride = (long long)a.Le * d;
+    const long long base = (slice * a.T * a.Le + (l - 1)) * (long long)d + lane * kCols;
+    const long long first = (long long)grp * a.B * stride;
+    float ak[kCols], av[kCols];
+#pragma unroll
+    for (int c = 0; c < kCols; c++) ak[c] = av[c] = 0.f;
+    constexpr int kUnroll = kCols >= 8 ? 2 : 16 / kCols;
+    for (int r0 = 0; r0 < a.B; r0 += kUnroll) {
+        float pk[kUnroll][kCols], pv[kUnroll][kCols];
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++) {
+            const bool ok = active && r0 + u < a.B;
+            const long long off = base + (first + (long long)(r0 + u) * stride) * rstride;
+            load_cols<kCols>(a.gK + (ok ? off : base), ok, pk[u]);
+            load_cols<kCols>(a.gV + (ok ? off : base), ok, pv[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; u++)
+#pragma unroll
+            for (int c = 0; c < kCols; c++) {
+                ak[c] += pk[u][c];
+                av[c] += pv[u][c];
+            }
+    }
+    if (active) {
+        const long long out = base + first * rstride;
+#pragma unroll
+        for (int c = 0; c < kCols; c++) {
+            a.gK[out + c] = ak[c];
+            a.gV[out + c] = av[c];
         }
     }
 }
@@ -567,8 +613,25 @@ void carve_bwd_workspace(const Shape& s, void* ws, AttnArgs* a) {
     a->dVc = reinterpret_cast<float*>(w);
 }
 
+template <int kCols>
+int launch_spans(const Shape& s, const AttnArgs& a, cudaStream_t st) {
+    int stride = 1, groups = s.T;
+    for (int step = 1; step < s.Le; step++) {
+        groups /= s.B;
+        const int warps = (s.Le - step) * groups;
+        const dim3 grid((warps + kReduceWarps - 1) / kReduceWarps, (unsigned)s.slices);
+        LLSA_LAUNCH("coarse_reduce", st, coarse_span_kernel<kCols><<<grid, 32 * kReduceWarps, 0, st>>>(a, step, stride, groups));
+        stride *= s.B;
+    }
+    return LLSA_OK;
+}
+
 int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     if (s.Le == 0) return LLSA_OK;
+    if (s.d <= 32) LLSA_TRY(launch_spans<1>(s, a, st));
+    else if (s.d <= 64) LLSA_TRY(launch_spans<2>(s, a, st));
+    else if (s.d <= 128) LLSA_TRY(launch_spans<4>(s, a, st));
+    else LLSA_TRY(launch_spans<8>(s, a, st));
     int rows = 0;
     for (int l = 1; l <= s.Le; l++) rows += s.n_level[l];
     const int gx = (rows + kReduceWarps - 1) / kReduceWarps;
