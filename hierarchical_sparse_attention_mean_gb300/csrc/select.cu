@@ -12,8 +12,9 @@
 // One launch per level, coarsest first (each level needs the one above). A CTA
 // owns up to 16 sibling query rows that share one candidate list: candidate
 // key rows are staged through shared memory in tiles of 32*KPL (coalesced
-// float4 loads), each warp scores one query row against the tile (a lane owns
-// KPL candidates; packed two-wide fp32 FMAs over even/odd columns), and the
+// float4 loads), the 16 warps score the CTA's rows against the tile as KPL
+// query rows x 32 candidates each (packed two-wide fp32 FMAs over even/odd
+// columns; a candidate row is read once per KPL query rows), and the
 // warp then runs K rounds of an arg-max tournament over its row's candidates
 // (each lane holding ceil(C/32) of them): scores map to order-preserving
 // unsigned keys, so a round is one warp max-reduction of the key and one
@@ -60,7 +61,7 @@ __device__ __forceinline__ unsigned order_key(float v) {
 }
 
 template <int CPL, int KPL>
-__global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs a) {
+__global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? 4 : 1) select_level_kernel(SelectArgs a) {
     constexpr int kTile = 32 * KPL;  // candidate rows per shared-memory tile
     extern __shared__ float4 smem4[];
     const int d = a.d, C = a.C;
@@ -110,24 +111,28 @@ __global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs 
                 __ldg(reinterpret_cast<const float4*>(kp + (long long)cand[t0 + r] * d) + c4);
         }
         __syncthreads();
-        if (warp < nrows) {
-            const float* qr = qrows + warp * d;
+        {
+            // warp = (row group, candidate group): KPL query rows against 32
+            // candidates, so each candidate row is read once per KPL query
+            // rows (query rows are broadcast reads)
+            const int rg = warp / KPL, cl = (warp % KPL) * 32 + lane;
+            const float* kr = ktile + cl * ktile_stride;
             float2 acc[KPL];
 #pragma unroll
-            for (int j = 0; j < KPL; j++) acc[j] = make_float2(0.f, 0.f);
+            for (int r = 0; r < KPL; r++) acc[r] = make_float2(0.f, 0.f);
             for (int c = 0; c < d; c += 4) {
-                const float4 q4 = *reinterpret_cast<const float4*>(qr + c);
-                const float2 qa = make_float2(q4.x, q4.y), qb = make_float2(q4.z, q4.w);
+                const float4 k4 = *reinterpret_cast<const float4*>(kr + c);
+                const float2 ka = make_float2(k4.x, k4.y), kb = make_float2(k4.z, k4.w);
 #pragma unroll
-                for (int j = 0; j < KPL; j++) {
-                    const float4 k4 = *reinterpret_cast<const float4*>(ktile + (lane + 32 * j) * ktile_stride + c);
-                    acc[j] = __ffma2_rn(qa, make_float2(k4.x, k4.y), acc[j]);
-                    acc[j] = __ffma2_rn(qb, make_float2(k4.z, k4.w), acc[j]);
+                for (int r = 0; r < KPL; r++) {
+                    const float4 q4 = *reinterpret_cast<const float4*>(qrows + (rg * KPL + r) * d + c);
+                    acc[r] = __ffma2_rn(make_float2(q4.x, q4.y), ka, acc[r]);
+                    acc[r] = __ffma2_rn(make_float2(q4.z, q4.w), kb, acc[r]);
                 }
             }
 #pragma unroll
-            for (int j = 0; j < KPL; j++)
-                if (lane + 32 * j < tn) scores[warp * C + t0 + lane + 32 * j] = acc[j].x + acc[j].y;
+            for (int r = 0; r < KPL; r++)
+                if (rg * KPL + r < nrows && cl < tn) scores[(rg * KPL + r) * C + t0 + cl] = acc[r].x + acc[r].y;
         }
     }
     __syncthreads();
@@ -148,20 +153,45 @@ __global__ void __launch_bounds__(32 * kMaxRows) select_level_kernel(SelectArgs 
             idx[m] = INT_MAX;
         }
     }
-    unsigned taken = 0;
     int* krow = kept + warp * kMaxKeep;
-    for (int k = 0; k < a.Kl; k++) {
-        unsigned bk = 0u;
-        int bi = INT_MAX;
+    if constexpr (CPL <= 8) {
+        // each lane sorts its candidates best first (insertion sort in
+        // registers); a round then compares only the lanes' current heads
 #pragma unroll
-        for (int m = 0; m < CPL; m++)
-            if (!(taken >> m & 1u) && (key[m] > bk || (key[m] == bk && idx[m] < bi))) { bk = key[m]; bi = idx[m]; }
-        const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
-        const int wi = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bi : 0xffffffffu);
+        for (int i = 1; i < CPL; i++)
 #pragma unroll
-        for (int m = 0; m < CPL; m++)
-            if (idx[m] == wi) taken |= 1u << m;
-        if (lane == 0) krow[k] = wi;
+            for (int j = i; j > 0; j--)
+                if (key[j] > key[j - 1] || (key[j] == key[j - 1] && idx[j] < idx[j - 1])) {
+                    const unsigned tk = key[j]; key[j] = key[j - 1]; key[j - 1] = tk;
+                    const int ti = idx[j]; idx[j] = idx[j - 1]; idx[j - 1] = ti;
+                }
+        int head = 0;
+        for (int k = 0; k < a.Kl; k++) {
+            unsigned hk = 0u;
+            int hi = INT_MAX;
+#pragma unroll
+            for (int m = 0; m < CPL; m++)
+                if (head == m) { hk = key[m]; hi = idx[m]; }
+            const unsigned wk = __reduce_max_sync(0xffffffffu, hk);
+            const int wi = (int)__reduce_min_sync(0xffffffffu, hk == wk ? (unsigned)hi : 0xffffffffu);
+            if (hk == wk && hi == wi) head++;
+            if (lane == 0) krow[k] = wi;
+        }
+    } else {
+        unsigned taken = 0;
+        for (int k = 0; k < a.Kl; k++) {
+            unsigned bk = 0u;
+            int bi = INT_MAX;
+#pragma unroll
+            for (int m = 0; m < CPL; m++)
+                if (!(taken >> m & 1u) && (key[m] > bk || (key[m] == bk && idx[m] < bi))) { bk = key[m]; bi = idx[m]; }
+            const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
+            const int wi = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bi : 0xffffffffu);
+#pragma unroll
+            for (int m = 0; m < CPL; m++)
+                if (idx[m] == wi) taken |= 1u << m;
+            if (lane == 0) krow[k] = wi;
+        }
     }
     __syncwarp();
     const int row = row0 + warp;
@@ -194,7 +224,7 @@ int launch_level_kpl(const SelectArgs& a, long long slices, cudaStream_t st) {
         cudaFuncSetAttribute(select_level_kernel<CPL, KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     LLSA_LAUNCH("select_level", st,
                 select_level_kernel<CPL, KPL>
-                <<<dim3(grid_x, (unsigned)slices), 32 * a.rows_per_cta, smem, st>>>(a));
+                <<<dim3(grid_x, (unsigned)slices), 32 * kMaxRows, smem, st>>>(a));
     return LLSA_OK;
 }
 
