@@ -411,8 +411,9 @@ def reorder_rate(w, dev, peaks):
     workload's shape, outside the step: HBM GB/s of `llsa_reorder`."""
     from hierarchical_sparse_attention_mean_gb300 import llsa_reorder, Params
     side, s = int(round(math.sqrt(w.n))), int(round(math.sqrt(w.block)))
-    if side * side != w.n or s * s != w.block:
-        return {"unavailable": "the workload is not a square image with B = s^2"}
+    m = int(round(math.log(side) / math.log(s))) if side > 1 and s > 1 else 0
+    if side * side != w.n or s * s != w.block or s ** m != side:
+        return {"unavailable": "the tile order needs a square image of side s^m with B = s^2"}
     td = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     p = Params(w.batch, w.heads, w.n, w.d, block=w.block, topk=w.topk, dtype=w.dtype)
     x = torch.randn(w.batch, w.heads, w.n, w.d, device=dev, dtype=td)
