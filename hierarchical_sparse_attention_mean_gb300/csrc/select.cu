@@ -60,11 +60,13 @@ __device__ __forceinline__ unsigned order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-template <int CPL, int KPL>
-__global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? 4 : 1) select_level_kernel(SelectArgs a) {
+// DT: the head dimension as a compile-time constant (64 or 128: divisions
+// and the scoring loop resolve at compile time), or 0 for any d
+template <int CPL, int KPL, int DT>
+__global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? (DT > 0 ? 3 : 4) : 1) select_level_kernel(SelectArgs a) {
     constexpr int kTile = 32 * KPL;  // candidate rows per shared-memory tile
     extern __shared__ float4 smem4[];
-    const int d = a.d, C = a.C;
+    const int d = DT > 0 ? DT : a.d, C = a.C;
     const int ktile_stride = d + 4;
     float* ktile = reinterpret_cast<float*>(smem4);                 // [kTile][d+4]
     float* qrows = ktile + kTile * ktile_stride;                     // [rows][d]
@@ -209,30 +211,35 @@ __global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? 4 : 1) select_level_
     for (int q = lane; q < a.span; q += 32) crow[(long long)q * a.L] = top1;
 }
 
-template <int CPL, int KPL>
+template <int KPL>
 size_t level_smem(const SelectArgs& a) {
     return sizeof(float) * (32 * KPL * (a.d + 4) + kMaxRows * a.d + kMaxRows * a.C) +
            sizeof(int) * (a.C + kMaxRows * kMaxKeep);
 }
 
-template <int CPL, int KPL>
+template <int CPL, int KPL, int DT>
 int launch_level_kpl(const SelectArgs& a, long long slices, cudaStream_t st) {
     const int grid_x = (a.n_l + a.rows_per_cta - 1) / a.rows_per_cta;
-    const size_t smem = level_smem<CPL, KPL>(a);
+    const size_t smem = level_smem<KPL>(a);
     if (smem > 200 * 1024 || slices > 65535) return LLSA_ERR_UNSUPPORTED;
     if (smem > 48 * 1024)
-        cudaFuncSetAttribute(select_level_kernel<CPL, KPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(select_level_kernel<CPL, KPL, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     LLSA_LAUNCH("select_level", st,
-                select_level_kernel<CPL, KPL>
+                select_level_kernel<CPL, KPL, DT>
                 <<<dim3(grid_x, (unsigned)slices), 32 * kMaxRows, smem, st>>>(a));
     return LLSA_OK;
 }
 
-// four candidates per lane per tile where the tile fits, else two
+// four candidates per lane per tile where the tile fits, else two; d = 64
+// and d = 128 have their own instantiations
 template <int CPL>
 int launch_level(const SelectArgs& a, long long slices, cudaStream_t st) {
-    if (level_smem<CPL, 4>(a) <= 200 * 1024) return launch_level_kpl<CPL, 4>(a, slices, st);
-    return launch_level_kpl<CPL, 2>(a, slices, st);
+    if (level_smem<4>(a) <= 200 * 1024) {
+        if (a.d == 64) return launch_level_kpl<CPL, 4, 64>(a, slices, st);
+        if (a.d == 128) return launch_level_kpl<CPL, 4, 128>(a, slices, st);
+        return launch_level_kpl<CPL, 4, 0>(a, slices, st);
+    }
+    return launch_level_kpl<CPL, 2, 0>(a, slices, st);
 }
 
 }  // namespace
