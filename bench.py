@@ -471,6 +471,84 @@ def dense_comparator(w, dev, llsa_ms):
             "what": "torch scaled_dot_product_attention fwd+bwd, dense, same shape and dtype, random inputs"}
 
 
+# Throughput across the method's hyperparameters on the same inputs (the
+# pages' ablations vary K, B, L and L_e; only the step time is measured here):
+# (label, B, K, L (0: floor(log_B N - 1)), L_e (-1: all levels))
+SWEEP = [
+    ("B16-K8", 16, 8, 0, -1),
+    ("B16-K4", 16, 4, 0, -1),
+    ("B16-K16", 16, 16, 0, -1),
+    ("B16-K32", 16, 32, 0, -1),
+    ("B8-K8", 8, 8, 0, -1),
+    ("B32-K8", 32, 8, 0, -1),
+    ("B64-K8", 64, 8, 0, -1),
+    ("B16-K8-L2", 16, 8, 2, -1),
+    ("B16-K8-L1", 16, 8, 1, -1),
+    ("B16-K8-Le0", 16, 8, 0, 0),
+    ("B16-K8-Le1", 16, 8, 0, 1),
+    ("B16-K8-Le2", 16, 8, 0, 2),
+]
+
+
+def run_sweep(args):
+    """One JSON line: ms per fwd+bwd step for each SWEEP entry on the
+    workload's inputs, with the effective TFLOP/s (14 d per (query, key) pair)
+    and whether the attention kernels ran on the tensor cores."""
+    import dataclasses
+    import hierarchical_sparse_attention_mean_gb300 as llsa
+    from hierarchical_sparse_attention_mean_gb300 import build
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    w0 = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w0, threads=os.cpu_count() or 8)
+    shape = (w0.batch, w0.heads, w0.n, w0.d)
+    td = torch.bfloat16 if w0.dtype == "bf16" else torch.float32
+    d = {k: torch.from_numpy(v).to(td).reshape(shape).to(dev) for k, v in x.items()}
+    rows = []
+    for label, B, K, L, Le in SWEEP:
+        p = llsa.Params(w0.batch, w0.heads, w0.n, w0.d, block=B, topk=K, levels=L, enrich_levels=Le, dtype=w0.dtype)
+        try:
+            s = llsa.get_sizes(p)
+            b = llsa.Buffers(p, dev)
+            dq, dk, dv = (torch.empty_like(d["q"]) for _ in range(3))
+
+            def step():
+                llsa.forward(p, d["q"], d["k"], d["v"], b)
+                llsa.backward(p, d["q"], d["k"], d["v"], d["dout"], b, dq, dk, dv)
+
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            llsa.profile_reset()
+            llsa.profile_enable(True)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(args.sweep_steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+            llsa.profile_enable(False)
+            records = llsa.profile_read(cap=64 * args.sweep_steps + 64)
+            if llsa.llsa_get_status() != 0:
+                raise RuntimeError("device status set")
+        except (llsa.LLSAError, RuntimeError) as e:
+            rows.append({"config": label, "unavailable": str(e)})
+            continue
+        ms = e0.elapsed_time(e1) / args.sweep_steps
+        work = work_model(dataclasses.replace(w0, block=B, topk=K), s)
+        tc = sorted(llsa_tensor_kernels(records))
+        rows.append({"config": label, "block": B, "topk": K, "levels": s.levels, "enrich_levels": s.enrich_levels,
+                     "keys_per_query": s.keys_per_query, "ms_per_step": round(ms, 4),
+                     "tflops": round(work["step_flops"] / (ms * 1e-3) / 1e12, 2),
+                     "attention": "tensor cores (" + ", ".join(tc) + ")" if tc else "CUDA cores"})
+        del b, dq, dk, dv
+    return {"metric": "LLSA fwd+bwd ms per step across B, K, L and L_e", "unit": "ms", "n_gpus": 1,
+            "steps": args.sweep_steps, "warmup": 3, "dtype": w0.dtype, "data": "synthetic",
+            "config": {"workload": w0.name}, "sweep": rows}
+
+
 def llsa_tensor_kernels(records):
     return {kernel_key(n) for n, _ in records if n.endswith("_tc")}
 
@@ -556,7 +634,13 @@ def main():
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture of this build")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: one line of step times across B, K, L and L_e")
+    ap.add_argument("--sweep-steps", type=int, default=10)
     args = ap.parse_args()
+    if args.sweep:
+        print(json.dumps(run_sweep(args)), flush=True)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     ws, rank, local = dist_env()
