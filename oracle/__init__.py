@@ -66,19 +66,21 @@ def _load():
     lib.orc_pair_scores.argtypes = [_f64p, _f64p, ctypes.c_int, _i64p, _i64p, _ll, _f64p]
     lib.orc_select_all.argtypes = [_f64p, _f64p, _ll, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                    ctypes.c_int, _i32p, _i32p, _i32p, ctypes.POINTER(_ll)]
+    lib.orc_coarse_cols.argtypes = [_ll, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    lib.orc_coarse_cols.restype = ctypes.c_int
     lib.orc_fwd.argtypes = [_f32p, _f32p, _f32p, _f64p, _f64p, _ll, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                            ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_double,
+                            ctypes.c_int, ctypes.c_int, _i32p, _i32p, ctypes.c_int, _i32p, ctypes.c_double,
                             ctypes.c_void_p, _ll, _f64p, _f64p]
     lib.orc_transpose.argtypes = [_i32p, _ll, ctypes.c_int, _ll, _i32p, _i32p]
     lib.orc_bwd.argtypes = [_f32p, _f32p, _f32p, _f64p, _f64p, _f64p, _f64p, _f32p, _ll, ctypes.c_int,
                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p,
-                            ctypes.c_double, _f64p, _f64p, _f64p]
+                            ctypes.c_int, _i32p, ctypes.c_double, _f64p, _f64p, _f64p]
     lib.orc_bwd_dq_rows.argtypes = [_f32p, _f32p, _f32p, _f64p, _f64p, _f64p, _f64p, _f32p, _ll, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p,
-                                    ctypes.c_double, _i64p, _ll, _f64p]
+                                    ctypes.c_int, _i32p, ctypes.c_double, _i64p, _ll, _f64p]
     lib.orc_bwd_dkv_blocks.argtypes = [_f32p, _f32p, _f32p, _f64p, _f64p, _f64p, _f64p, _f32p, _ll, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p, _i32p,
-                                       ctypes.c_double, _i64p, _ll, _f64p, _f64p]
+                                       ctypes.c_int, _i32p, ctypes.c_double, _i64p, _ll, _f64p, _f64p]
     _lib = lib
     return lib
 
@@ -181,22 +183,44 @@ def pair_scores(qpyr_l, kpyr_l, rows, cols) -> np.ndarray:
     return out
 
 
-RULES = {"top1": 0, "ancestor": 1}
+RULES = {"top1": 0, "ancestor": 1, "allk": 2}
+
+
+def coarse_levels(n: int, B: int, L: int, K: int, rule: str = "top1") -> np.ndarray:
+    """Level (1..L) of each column of a query block's enrichment row: one
+    column per level for "top1" and "ancestor", K_l columns for level l under
+    "allk"."""
+    lib = _load()
+    ncol = _check(lib.orc_coarse_cols(n, B, L, K, RULES[rule], None), "coarse_cols")
+    clev = np.empty(ncol, np.int32)
+    lib.orc_coarse_cols(n, B, L, K, RULES[rule], clev.ctypes.data)
+    return clev
+
+
+def _clev(coarse, L, clev):
+    """The column levels of a coarse table: given, or one column per level."""
+    if clev is not None:
+        return _i32(clev)
+    if coarse.shape[1] != L:
+        raise ValueError("coarse has more columns than levels: pass clev")
+    return np.arange(1, L + 1, dtype=np.int32)
 
 
 def select_all(qpyr, kpyr, n: int, B: int, L: int, K: int, rule: str = "top1") -> dict:
     """All levels coarsest-first plus the enrichment index (rule "top1": the
     rank-1 selection of the query block's level-l ancestor; "ancestor": that
-    ancestor itself).
+    ancestor itself; "allk": all K_l selections of level l for that ancestor).
     Returns {'levels': [None, I1, ..., IL], 'top1': [None, t1, ...],
-             'coarse': int32 [n_1, L], 'work': scored pairs}."""
+             'coarse': int32 [n_1, C], 'clev': int32 [C] (column levels),
+             'work': scored pairs}."""
     qpyr, kpyr = _f64(qpyr), _f64(kpyr)
     d = qpyr.shape[1]
     sizes = level_sizes(n, B, L)
     kl = level_topk(n, B, L, K)
     idx_all = np.empty(sum(sizes[l] * kl[l] for l in range(1, L + 1)), np.int32)
     top1_all = np.empty(sum(sizes[1:]), np.int32)
-    coarse = np.empty((sizes[1], L), np.int32)
+    clev = coarse_levels(n, B, L, K, rule)
+    coarse = np.empty((sizes[1], clev.size), np.int32)
     work = _ll(0)
     _check(_load().orc_select_all(qpyr, kpyr, n, d, B, L, K, RULES[rule], idx_all, top1_all, coarse,
                                   ctypes.byref(work)),
@@ -208,12 +232,13 @@ def select_all(qpyr, kpyr, n: int, B: int, L: int, K: int, rule: str = "top1") -
         top1.append(top1_all[to:to + sizes[l]])
         io += sizes[l] * kl[l]
         to += sizes[l]
-    return {"levels": levels, "top1": top1, "coarse": coarse, "work": int(work.value)}
+    return {"levels": levels, "top1": top1, "coarse": coarse, "clev": clev, "work": int(work.value)}
 
 
-def fwd(q, k, v, kpyr, vpyr, B, L, Le, sel, coarse, scale, qlist=None):
+def fwd(q, k, v, kpyr, vpyr, B, L, Le, sel, coarse, scale, qlist=None, clev=None):
     """Forward of one slice; returns (o float64 [rows, d], lse float64 [rows])
-    for all tokens, or for the tokens in qlist (in list order)."""
+    for all tokens, or for the tokens in qlist (in list order). clev: the
+    levels of coarse's columns (default: one column per level)."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     kpyr, vpyr = _f64(kpyr), _f64(vpyr)
     sel, coarse = _i32(sel), _i32(coarse)
@@ -225,8 +250,9 @@ def fwd(q, k, v, kpyr, vpyr, B, L, Le, sel, coarse, scale, qlist=None):
         nq, qptr = keep.size, keep.ctypes.data
     o = np.empty((nq, d), np.float64)
     lse = np.empty(nq, np.float64)
-    _check(_load().orc_fwd(q, k, v, kpyr, vpyr, n, d, B, L, Le, sel.shape[1], sel, coarse, float(scale),
-                           qptr, nq, o, lse), "fwd")
+    cl = _clev(coarse, L, clev)
+    _check(_load().orc_fwd(q, k, v, kpyr, vpyr, n, d, B, L, Le, sel.shape[1], sel, coarse, cl.size, cl,
+                           float(scale), qptr, nq, o, lse), "fwd")
     return o, lse
 
 
@@ -240,31 +266,34 @@ def transpose(sel, ncols: int):
     return col_ptr, row_idx
 
 
-def bwd(q, k, v, kpyr, vpyr, o, lse, dout, B, L, Le, sel, coarse, scale):
+def bwd(q, k, v, kpyr, vpyr, o, lse, dout, B, L, Le, sel, coarse, scale, clev=None):
     """Backward of one slice; returns (dq, dk, dv) float64 [n, d]."""
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
     n, d = q.shape
     dq, dk, dv = (np.empty((n, d), np.float64) for _ in range(3))
     sel, coarse = _i32(sel), _i32(coarse)
+    cl = _clev(coarse, L, clev)
     _check(_load().orc_bwd(q, k, v, _f64(kpyr), _f64(vpyr), _f64(o), _f64(lse), dout, n, d, B, L, Le,
-                           sel.shape[1], sel, coarse, float(scale), dq, dk, dv), "bwd")
+                           sel.shape[1], sel, coarse, cl.size, cl, float(scale), dq, dk, dv), "bwd")
     return dq, dk, dv
 
 
-def bwd_dq_rows(q, k, v, kpyr, vpyr, o_rows, lse_rows, dout, B, L, Le, sel, coarse, scale, qlist):
+def bwd_dq_rows(q, k, v, kpyr, vpyr, o_rows, lse_rows, dout, B, L, Le, sel, coarse, scale, qlist, clev=None):
     """dq of the listed tokens only (o_rows, lse_rows in list order)."""
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
     n, d = q.shape
     ql = np.ascontiguousarray(qlist, np.int64)
     out = np.empty((ql.size, d), np.float64)
     sel, coarse = _i32(sel), _i32(coarse)
+    cl = _clev(coarse, L, clev)
     _check(_load().orc_bwd_dq_rows(q, k, v, _f64(kpyr), _f64(vpyr), _f64(o_rows), _f64(lse_rows), dout, n, d,
-                                   B, L, Le, sel.shape[1], sel, coarse, float(scale), ql, ql.size, out),
+                                   B, L, Le, sel.shape[1], sel, coarse, cl.size, cl, float(scale), ql, ql.size,
+                                   out),
            "bwd_dq_rows")
     return out
 
 
-def bwd_dkv_blocks(q, k, v, kpyr, vpyr, o, lse, dout, B, L, Le, sel, coarse, scale, kblocks):
+def bwd_dkv_blocks(q, k, v, kpyr, vpyr, o, lse, dout, B, L, Le, sel, coarse, scale, kblocks, clev=None):
     """dk, dv of the fine tokens of the listed key blocks: [len*B, d] each."""
     q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
     n, d = q.shape
@@ -272,8 +301,10 @@ def bwd_dkv_blocks(q, k, v, kpyr, vpyr, o, lse, dout, B, L, Le, sel, coarse, sca
     dk = np.empty((kb.size * B, d), np.float64)
     dv = np.empty((kb.size * B, d), np.float64)
     sel, coarse = _i32(sel), _i32(coarse)
+    cl = _clev(coarse, L, clev)
     _check(_load().orc_bwd_dkv_blocks(q, k, v, _f64(kpyr), _f64(vpyr), _f64(o), _f64(lse), dout, n, d, B, L,
-                                      Le, sel.shape[1], sel, coarse, float(scale), kb, kb.size, dk, dv),
+                                      Le, sel.shape[1], sel, coarse, cl.size, cl, float(scale), kb, kb.size, dk,
+                                      dv),
            "bwd_dkv_blocks")
     return dk, dv
 
@@ -304,14 +335,14 @@ def run(q, k, v, dout=None, *, B=16, K=8, L=None, Le=None, scale=None, threads=1
     def one(s):
         qp, kp, vp = pool(q3[s], B, L), pool(k3[s], B, L), pool(v3[s], B, L)
         sel = select_all(qp, kp, n, B, L, K, rule)
-        I1, coarse = sel["levels"][1], sel["coarse"]
-        o, lse = fwd(q3[s], k3[s], v3[s], kp, vp, B, L, Le, I1, coarse, scale)
+        I1, coarse, clev = sel["levels"][1], sel["coarse"], sel["clev"]
+        o, lse = fwd(q3[s], k3[s], v3[s], kp, vp, B, L, Le, I1, coarse, scale, clev=clev)
         col_ptr, row_idx = transpose(I1, T)
         res = {"qpyr": qp, "kpyr": kp, "vpyr": vp, "sel": sel, "o": o, "lse": lse,
                "col_ptr": col_ptr, "row_idx": row_idx}
         if do3 is not None and backward:
             res["dq"], res["dk"], res["dv"] = bwd(q3[s], k3[s], v3[s], kp, vp, o, lse, do3[s], B, L, Le,
-                                                  I1, coarse, scale)
+                                                  I1, coarse, scale, clev=clev)
         return res
 
     if threads > 1 and bh > 1:

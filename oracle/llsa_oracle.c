@@ -45,6 +45,7 @@
 #define ORC_OK 0
 #define ORC_ERR_ARG (-1)
 #define ORC_ERR_MEM (-2)
+#define ORC_MAX_COARSE 512 /* coarse columns per query block */
 
 /* ------------------------------------------------------------------------ */
 /* Level bookkeeping ("What carries the argument": L = floor(log_B N - 1)).  */
@@ -210,15 +211,39 @@ int orc_pair_scores(const double *qpyr_l, const double *kpyr_l, int d,
     return ORC_OK;
 }
 
+/* The coarse-token columns of a query block's enrichment row, levels 1..L
+ * in order: one column per level for TOP1 (rule 0) and ANCESTOR (rule 1), K_l
+ * columns for level l under ALLK (rule 2: every token level l keeps for the
+ * block's ancestor). Fills clev[c] = level of column c (when clev is not
+ * NULL) and returns the column count, or a negative error. */
+int orc_coarse_cols(long long n, int B, int L, int K, int rule, int *clev)
+{
+    int kl[64];
+    if (L < 1 || L > 60 || orc_level_topk(n, B, L, K, kl) != ORC_OK) return ORC_ERR_ARG;
+    if (rule < 0 || rule > 2) return ORC_ERR_ARG;
+    int c = 0;
+    for (int l = 1; l <= L; l++) {
+        int cnt = rule == 2 ? kl[l] : 1;
+        for (int r = 0; r < cnt; r++) {
+            if (c >= ORC_MAX_COARSE) return ORC_ERR_ARG;
+            if (clev) clev[c] = l;
+            c++;
+        }
+    }
+    return c;
+}
+
 /* All levels, coarsest first, plus the enrichment index.
  *   qpyr, kpyr : pyramids (levels 1..L one after another).
- *   rule       : 0 (TOP1) or 1 (ANCESTOR), see coarse.
+ *   rule       : 0 (TOP1), 1 (ANCESTOR) or 2 (ALLK), see coarse.
  *   idx_all    : level 1 first: n_1*K_1 ints, then n_2*K_2, ... n_L*K_L.
  *   top1_all   : n_1 + ... + n_L rank-1 indices, level 1 first.
- *   coarse     : n_1 rows of L entries; coarse[i*L + (l-1)] is the level-l
- *                enrichment token of query block i: for TOP1 the rank-1
- *                selection of level l for i's ancestor floor(i / B^(l-1)),
- *                for ANCESTOR that ancestor itself.
+ *   coarse     : n_1 rows of orc_coarse_cols(...) entries. The level-l columns
+ *                of query block i hold its level-l enrichment tokens: for TOP1
+ *                the rank-1 selection of level l for i's ancestor
+ *                floor(i / B^(l-1)), for ANCESTOR that ancestor itself, for
+ *                ALLK all K_l selections of level l for that ancestor
+ *                (ascending, as the level's row is stored).
  *   work_out   : number of scored candidate pairs over all levels. */
 int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, int B, int L, int K, int rule,
                    int *idx_all, int *top1_all, int *coarse, long long *work_out)
@@ -227,7 +252,8 @@ int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, i
     int kl[64];
     if (L < 1 || L > 60 || orc_level_sizes(n, B, L, nl) != ORC_OK) return ORC_ERR_ARG;
     if (orc_level_topk(n, B, L, K, kl) != ORC_OK) return ORC_ERR_ARG;
-    if (rule != 0 && rule != 1) return ORC_ERR_ARG;
+    const int ncol = orc_coarse_cols(n, B, L, K, rule, NULL);
+    if (ncol < 0) return ORC_ERR_ARG;
     long long row_off[64], idx_off[64], t1_off[64];
     row_off[1] = 0; idx_off[1] = 0; t1_off[1] = 0;
     for (int l = 2; l <= L; l++) {
@@ -244,9 +270,17 @@ int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, i
         if (r != kl[l]) return r < 0 ? r : ORC_ERR_ARG;
     }
     long long span = 1;
+    int c0 = 0;
     for (int l = 1; l <= L; l++) {
-        for (long long i = 0; i < nl[1]; i++)
-            coarse[i * L + (l - 1)] = rule == 1 ? (int)(i / span) : top1_all[t1_off[l] + i / span];
+        int cnt = rule == 2 ? kl[l] : 1;
+        for (long long i = 0; i < nl[1]; i++) {
+            long long anc = i / span;
+            for (int r = 0; r < cnt; r++)
+                coarse[i * ncol + c0 + r] = rule == 0 ? top1_all[t1_off[l] + anc]
+                                            : rule == 1 ? (int)anc
+                                                        : idx_all[idx_off[l] + anc * kl[l] + r];
+        }
+        c0 += cnt;
         span *= B;
     }
     return ORC_OK;
@@ -257,13 +291,15 @@ int orc_select_all(const double *qpyr, const double *kpyr, long long n, int d, i
 /* ------------------------------------------------------------------------ */
 
 /* The key set of query block i: the B fine tokens of each selected level-1
- * block, then one coarse token per enrichment level l = 1..Le with logit
- * offset ln(B^l). Fills key rows (pointers) and offsets; returns the count. */
+ * block (kf, vf), then the coarse tokens of the enrichment levels 1..Le:
+ * every column c of i's coarse row with clev[c] <= Le, with logit offset
+ * ln(B^l), l = clev[c] (kc, vc, bias_c; crow[m] = its pyramid row). Returns
+ * the number of coarse keys. */
 static int key_set(const float *k, const float *v, const double *kpyr, const double *vpyr,
-                   const long long *row_off, int d, int B, int Le, int L, int K1,
-                   const int *sel, const int *coarse, long long i,
+                   const long long *row_off, int d, int B, int Le, int K1,
+                   const int *sel, const int *coarse, int ncol, const int *clev, long long i,
                    const float **kf, const float **vf, const double **kc, const double **vc,
-                   double *bias_c)
+                   double *bias_c, long long *crow)
 {
     int nf = 0;
     for (int m = 0; m < K1; m++) {
@@ -274,13 +310,30 @@ static int key_set(const float *k, const float *v, const double *kpyr, const dou
             nf++;
         }
     }
-    for (int l = 1; l <= Le; l++) {
-        long long e = coarse[i * L + (l - 1)];
-        kc[l - 1] = kpyr + (row_off[l] + e) * d;
-        vc[l - 1] = vpyr + (row_off[l] + e) * d;
-        bias_c[l - 1] = (double)l * log((double)B);
+    int nc = 0;
+    for (int c = 0; c < ncol; c++) {
+        int l = clev[c];
+        if (l > Le) continue;
+        long long row = row_off[l] + coarse[i * ncol + c];
+        kc[nc] = kpyr + row * d;
+        vc[nc] = vpyr + row * d;
+        bias_c[nc] = (double)l * log((double)B);
+        crow[nc] = row;
+        nc++;
     }
-    return nf;
+    return nc;
+}
+
+/* A coarse row description is valid: ncol columns, levels nondecreasing in
+ * 1..L (columns of the levels 1..Le come first). */
+static int coarse_ok(int ncol, const int *clev, int L)
+{
+    if (ncol < 0 || ncol > ORC_MAX_COARSE) return 0;
+    for (int c = 0; c < ncol; c++) {
+        if (clev[c] < 1 || clev[c] > L) return 0;
+        if (c > 0 && clev[c] < clev[c - 1]) return 0;
+    }
+    return 1;
 }
 
 static double dot_fd(const float *a, const float *b, int d)
@@ -300,36 +353,40 @@ static double dot_fD(const float *a, const double *b, int d)
 /* Forward for the query tokens in qlist (all n tokens when qlist is NULL).
  * For token t in block i = t/B:
  *   s_j = scale * q_t . k_j            for the fine keys j,
- *   s_l = scale * q_t . K^(l)[e_l(i)] + ln(B^l)   for l = 1..Le,
- *   lse_t = ln(sum_j e^{s_j} + sum_l e^{s_l}),
- *   o_t = sum_j e^{s_j - lse_t} v_j + sum_l e^{s_l - lse_t} V^(l)[e_l(i)].
+ *   s_x = scale * q_t . K^(l)[e] + ln(B^l)   for each coarse key x = (l, e) of
+ *                                             the enrichment levels l = 1..Le,
+ *   lse_t = ln(sum_j e^{s_j} + sum_x e^{s_x}),
+ *   o_t = sum_j e^{s_j - lse_t} v_j + sum_x e^{s_x - lse_t} V^(l)[e].
+ * coarse: n_1 rows of ncol columns, clev[c] the level of column c.
  * Outputs are compacted: o[r*d..], lse[r] for the r-th listed token. */
 int orc_fwd(const float *q, const float *k, const float *v, const double *kpyr, const double *vpyr,
             long long n, int d, int B, int L, int Le, int K1, const int *sel, const int *coarse,
-            double scale, const long long *qlist, long long nq, double *o, double *lse)
+            int ncol, const int *clev, double scale, const long long *qlist, long long nq, double *o, double *lse)
 {
     long long nl[64], row_off[64];
     if (L < 1 || L > 60 || Le < 0 || Le > L || orc_level_sizes(n, B, L, nl) != ORC_OK) return ORC_ERR_ARG;
+    if (!coarse_ok(ncol, clev, L)) return ORC_ERR_ARG;
     row_off[1] = 0;
     for (int l = 2; l <= L; l++) row_off[l] = row_off[l - 1] + nl[l - 1];
     int nkf = K1 * B;
     const float **kf = (const float **)malloc(sizeof(void *) * nkf);
     const float **vf = (const float **)malloc(sizeof(void *) * nkf);
-    const double *kc[64], *vc[64];
-    double bias[64];
-    double *s = (double *)malloc(sizeof(double) * (nkf + Le + 1));
+    const double *kc[ORC_MAX_COARSE], *vc[ORC_MAX_COARSE];
+    double bias[ORC_MAX_COARSE];
+    long long crow[ORC_MAX_COARSE];
+    double *s = (double *)malloc(sizeof(double) * (nkf + ncol + 1));
     if (!kf || !vf || !s) { free(kf); free(vf); free(s); return ORC_ERR_MEM; }
     long long count = qlist ? nq : n;
     for (long long r = 0; r < count; r++) {
         long long t = qlist ? qlist[r] : r;
         long long i = t / B;
-        key_set(k, v, kpyr, vpyr, row_off, d, B, Le, L, K1, sel, coarse, i, kf, vf, kc, vc, bias);
+        int nc = key_set(k, v, kpyr, vpyr, row_off, d, B, Le, K1, sel, coarse, ncol, clev, i, kf, vf, kc, vc, bias, crow);
         const float *qt = q + t * d;
         double m = -INFINITY;
         for (int j = 0; j < nkf; j++) { s[j] = scale * dot_fd(qt, kf[j], d); if (s[j] > m) m = s[j]; }
-        for (int l = 0; l < Le; l++) { s[nkf + l] = scale * dot_fD(qt, kc[l], d) + bias[l]; if (s[nkf + l] > m) m = s[nkf + l]; }
+        for (int x = 0; x < nc; x++) { s[nkf + x] = scale * dot_fD(qt, kc[x], d) + bias[x]; if (s[nkf + x] > m) m = s[nkf + x]; }
         double z = 0.0;
-        for (int j = 0; j < nkf + Le; j++) z += exp(s[j] - m);
+        for (int j = 0; j < nkf + nc; j++) z += exp(s[j] - m);
         double lt = m + log(z);
         lse[r] = lt;
         double *ot = o + r * d;
@@ -338,9 +395,9 @@ int orc_fwd(const float *q, const float *k, const float *v, const double *kpyr, 
             double p = exp(s[j] - lt);
             for (int c = 0; c < d; c++) ot[c] += p * (double)vf[j][c];
         }
-        for (int l = 0; l < Le; l++) {
-            double p = exp(s[nkf + l] - lt);
-            for (int c = 0; c < d; c++) ot[c] += p * vc[l][c];
+        for (int x = 0; x < nc; x++) {
+            double p = exp(s[nkf + x] - lt);
+            for (int c = 0; c < d; c++) ot[c] += p * vc[x][c];
         }
     }
     free(kf); free(vf); free(s);
@@ -385,15 +442,16 @@ int orc_transpose(const int *sel, long long T, int K, long long ncols, int *col_
  *   dq_t += scale dS k_x,  dk_x += scale dS q_t,  dv_x += P dO_t,
  * where a coarse key x = K^(l)[e] accumulates into dK^(l)[e], dV^(l)[e].
  * Then, since K^(l)[e] is the mean of the B^l fine rows it covers,
- *   dk_t += sum_l dK^(l)[t / B^l] / B^l   (same for dv).
+ *   dk_t += sum_l dK^(l)[t / B^l] / B^l   (same for dv), l = 1..Le.
  * o and lse are this oracle's own forward results for all n tokens. */
 int orc_bwd(const float *q, const float *k, const float *v, const double *kpyr, const double *vpyr,
             const double *o, const double *lse, const float *dout,
             long long n, int d, int B, int L, int Le, int K1, const int *sel, const int *coarse,
-            double scale, double *dq, double *dk, double *dv)
+            int ncol, const int *clev, double scale, double *dq, double *dk, double *dv)
 {
     long long nl[64], row_off[64];
     if (L < 1 || L > 60 || Le < 0 || Le > L || orc_level_sizes(n, B, L, nl) != ORC_OK) return ORC_ERR_ARG;
+    if (!coarse_ok(ncol, clev, L)) return ORC_ERR_ARG;
     row_off[1] = 0;
     long long P = nl[1];
     for (int l = 2; l <= L; l++) { row_off[l] = row_off[l - 1] + nl[l - 1]; P += nl[l]; }
@@ -403,8 +461,9 @@ int orc_bwd(const float *q, const float *k, const float *v, const double *kpyr, 
     long long *kfi = (long long *)malloc(sizeof(long long) * nkf);
     double *dkc = (double *)calloc((size_t)(P * d), sizeof(double));
     double *dvc = (double *)calloc((size_t)(P * d), sizeof(double));
-    const double *kc[64], *vc[64];
-    double bias[64];
+    const double *kc[ORC_MAX_COARSE], *vc[ORC_MAX_COARSE];
+    double bias[ORC_MAX_COARSE];
+    long long crow[ORC_MAX_COARSE];
     if (!kf || !vf || !kfi || !dkc || !dvc) {
         free(kf); free(vf); free(kfi); free(dkc); free(dvc);
         return ORC_ERR_MEM;
@@ -414,7 +473,7 @@ int orc_bwd(const float *q, const float *k, const float *v, const double *kpyr, 
     memset(dv, 0, sizeof(double) * n * d);
     for (long long t = 0; t < n; t++) {
         long long i = t / B;
-        key_set(k, v, kpyr, vpyr, row_off, d, B, Le, L, K1, sel, coarse, i, kf, vf, kc, vc, bias);
+        int nc = key_set(k, v, kpyr, vpyr, row_off, d, B, Le, K1, sel, coarse, ncol, clev, i, kf, vf, kc, vc, bias, crow);
         for (int m = 0; m < K1; m++)
             for (int c = 0; c < B; c++) kfi[m * B + c] = (long long)sel[i * K1 + m] * B + c;
         const float *qt = q + t * d;
@@ -433,17 +492,16 @@ int orc_bwd(const float *q, const float *k, const float *v, const double *kpyr, 
                 dv[x * d + c] += p * (double)gt[c];
             }
         }
-        for (int l = 1; l <= Le; l++) {
-            long long e = coarse[i * L + (l - 1)];
-            double s = scale * dot_fD(qt, kc[l - 1], d) + bias[l - 1];
+        for (int x = 0; x < nc; x++) {
+            double s = scale * dot_fD(qt, kc[x], d) + bias[x];
             double p = exp(s - lse[t]);
             double dp = 0.0;
-            for (int c = 0; c < d; c++) dp += (double)gt[c] * vc[l - 1][c];
+            for (int c = 0; c < d; c++) dp += (double)gt[c] * vc[x][c];
             double ds = p * (dp - Dt);
-            double *gk = dkc + (row_off[l] + e) * d;
-            double *gv = dvc + (row_off[l] + e) * d;
+            double *gk = dkc + crow[x] * d;
+            double *gv = dvc + crow[x] * d;
             for (int c = 0; c < d; c++) {
-                dq[t * d + c] += scale * ds * kc[l - 1][c];
+                dq[t * d + c] += scale * ds * kc[x][c];
                 gk[c] += scale * ds * (double)qt[c];
                 gv[c] += p * (double)gt[c];
             }
@@ -471,22 +529,24 @@ int orc_bwd(const float *q, const float *k, const float *v, const double *kpyr, 
 int orc_bwd_dq_rows(const float *q, const float *k, const float *v, const double *kpyr, const double *vpyr,
                     const double *o_rows, const double *lse_rows, const float *dout,
                     long long n, int d, int B, int L, int Le, int K1, const int *sel, const int *coarse,
-                    double scale, const long long *qlist, long long nq, double *dq_rows)
+                    int ncol, const int *clev, double scale, const long long *qlist, long long nq, double *dq_rows)
 {
     long long nl[64], row_off[64];
     if (L < 1 || L > 60 || Le < 0 || Le > L || orc_level_sizes(n, B, L, nl) != ORC_OK) return ORC_ERR_ARG;
+    if (!coarse_ok(ncol, clev, L)) return ORC_ERR_ARG;
     row_off[1] = 0;
     for (int l = 2; l <= L; l++) row_off[l] = row_off[l - 1] + nl[l - 1];
     int nkf = K1 * B;
     const float **kf = (const float **)malloc(sizeof(void *) * nkf);
     const float **vf = (const float **)malloc(sizeof(void *) * nkf);
-    const double *kc[64], *vc[64];
-    double bias[64];
+    const double *kc[ORC_MAX_COARSE], *vc[ORC_MAX_COARSE];
+    double bias[ORC_MAX_COARSE];
+    long long crow[ORC_MAX_COARSE];
     if (!kf || !vf) { free(kf); free(vf); return ORC_ERR_MEM; }
     for (long long r = 0; r < nq; r++) {
         long long t = qlist[r];
         long long i = t / B;
-        key_set(k, v, kpyr, vpyr, row_off, d, B, Le, L, K1, sel, coarse, i, kf, vf, kc, vc, bias);
+        int nc = key_set(k, v, kpyr, vpyr, row_off, d, B, Le, K1, sel, coarse, ncol, clev, i, kf, vf, kc, vc, bias, crow);
         const float *qt = q + t * d;
         const float *gt = dout + t * d;
         double *g = dq_rows + r * d;
@@ -497,12 +557,12 @@ int orc_bwd_dq_rows(const float *q, const float *k, const float *v, const double
             double ds = p * (dot_fd(gt, vf[j], d) - Dt);
             for (int c = 0; c < d; c++) g[c] += scale * ds * (double)kf[j][c];
         }
-        for (int l = 0; l < Le; l++) {
-            double p = exp(scale * dot_fD(qt, kc[l], d) + bias[l] - lse_rows[r]);
+        for (int x = 0; x < nc; x++) {
+            double p = exp(scale * dot_fD(qt, kc[x], d) + bias[x] - lse_rows[r]);
             double dp = 0.0;
-            for (int c = 0; c < d; c++) dp += (double)gt[c] * vc[l][c];
+            for (int c = 0; c < d; c++) dp += (double)gt[c] * vc[x][c];
             double ds = p * (dp - Dt);
-            for (int c = 0; c < d; c++) g[c] += scale * ds * kc[l][c];
+            for (int c = 0; c < d; c++) g[c] += scale * ds * kc[x][c];
         }
     }
     free(kf); free(vf);
@@ -511,16 +571,19 @@ int orc_bwd_dq_rows(const float *q, const float *k, const float *v, const double
 
 /* dk, dv for the fine tokens of the listed key blocks (block j covers tokens
  * jB..jB+B-1). Every query block whose selection contains j contributes its
- * fine pairs; every query block whose level-l enrichment token is the level-l
- * ancestor of j contributes through the mean, divided by B^l. o and lse are
- * the forward results for ALL n tokens. Output rows: nkb*B rows of d. */
+ * fine pairs; every query block with the level-l ancestor of j among its
+ * level-l enrichment tokens contributes through the mean, divided by B^l. o
+ * and lse are the forward results for ALL n tokens. Output rows: nkb*B rows
+ * of d. */
 int orc_bwd_dkv_blocks(const float *q, const float *k, const float *v, const double *kpyr, const double *vpyr,
                        const double *o, const double *lse, const float *dout,
                        long long n, int d, int B, int L, int Le, int K1, const int *sel, const int *coarse,
-                       double scale, const long long *kblocks, long long nkb, double *dk_rows, double *dv_rows)
+                       int ncol, const int *clev, double scale, const long long *kblocks, long long nkb,
+                       double *dk_rows, double *dv_rows)
 {
     long long nl[64], row_off[64];
     if (L < 1 || L > 60 || Le < 0 || Le > L || orc_level_sizes(n, B, L, nl) != ORC_OK) return ORC_ERR_ARG;
+    if (!coarse_ok(ncol, clev, L)) return ORC_ERR_ARG;
     row_off[1] = 0;
     for (int l = 2; l <= L; l++) row_off[l] = row_off[l - 1] + nl[l - 1];
     long long T = nl[1];
@@ -563,7 +626,10 @@ int orc_bwd_dkv_blocks(const float *q, const float *k, const float *v, const dou
             double bias = (double)l * log((double)B);
             for (int c = 0; c < d; c++) { gk[c] = 0.0; gv[c] = 0.0; }
             for (long long i = 0; i < T; i++) {
-                if (coarse[i * L + (l - 1)] != e) continue;
+                int has = 0;
+                for (int c = 0; c < ncol; c++)
+                    if (clev[c] == l && coarse[i * ncol + c] == e) has = 1;
+                if (!has) continue;
                 for (int r = 0; r < B; r++) {
                     long long t = i * B + r;
                     const float *qt = q + t * d;

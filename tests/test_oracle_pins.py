@@ -51,10 +51,12 @@ def brute_topk(scores, cand, K):
     return sorted(keep), top1
 
 
-def dense_masked(q, k, v, B, L, Le, sel, coarse, scale):
+def dense_masked(q, k, v, B, L, Le, sel, coarse, scale, clev=None):
     """Brute-force attention: one dense logit matrix over all n fine tokens and
     all pooled tokens of levels 1..Le, masked to the sparse key set (0 / -inf)
-    plus ln(B^l) on the coarse columns; softmax by logsumexp."""
+    plus ln(B^l) on the coarse columns; softmax by logsumexp. clev: level of
+    each column of coarse (default one column per level)."""
+    clev = list(range(1, L + 1)) if clev is None else [int(c) for c in clev]
     q64, k64, v64 = (np.asarray(a, np.float64) for a in (q, k, v))
     n, d = q64.shape
     kp, vp = direct_mean_pyramid(k, B, L), direct_mean_pyramid(v, B, L)
@@ -70,8 +72,9 @@ def dense_masked(q, k, v, B, L, Le, sel, coarse, scale):
         i = t // B
         for j in sel[i]:
             mask[t, j * B:(j + 1) * B] = 0.0
-        for l in range(1, Le + 1):
-            mask[t, col0[l] + coarse[i, l - 1]] = l * math.log(B)
+        for c, l in enumerate(clev):
+            if l <= Le:
+                mask[t, col0[l] + coarse[i, c]] = l * math.log(B)
     z = logits + mask
     m = z.max(axis=1, keepdims=True)
     lse = (m + np.log(np.exp(z - m).sum(axis=1, keepdims=True)))[:, 0]
@@ -377,9 +380,10 @@ def test_backward_central_finite_differences():
             assert abs(fd - grads[name][t, c]) <= 1e-5 * max(1.0, abs(fd)), (name, t, c, fd, grads[name][t, c])
 
 
-def _torch_masked_grads(x, B, L, Le, sel, coarse, scale):
+def _torch_masked_grads(x, B, L, Le, sel, coarse, scale, clev=None):
     """Autograd of the dense-mask formulation; pooled K, V are torch means of
     the fine rows, so their gradient reaches the fine rows through autograd."""
+    clev = list(range(1, L + 1)) if clev is None else [int(c) for c in clev]
     q, k, v, do = (torch.tensor(x[a][0], dtype=torch.float64, requires_grad=(a != "dout"))
                    for a in ("q", "k", "v", "dout"))
     n, d = q.shape
@@ -394,8 +398,9 @@ def _torch_masked_grads(x, B, L, Le, sel, coarse, scale):
         i = t // B
         for j in sel[i]:
             mask[t, j * B:(j + 1) * B] = 0.0
-        for l in range(1, Le + 1):
-            mask[t, col0[l] + coarse[i, l - 1]] = l * math.log(B)
+        for c, l in enumerate(clev):
+            if l <= Le:
+                mask[t, col0[l] + coarse[i, c]] = l * math.log(B)
     z = scale * q @ K_all.T + mask
     o = torch.softmax(z, 1) @ V_all
     (o * do).sum().backward()
@@ -518,6 +523,80 @@ def test_ancestor_full_selection_closed_form():
     o = p[:, :n] @ v + p[:, n:] * vc.repeat_interleave(B, 0)
     np.testing.assert_allclose(res["slices"][0]["o"], o.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(res["slices"][0]["lse"], lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# -------------------------------------------------------- ALLK enrichment ---
+
+def test_allk_with_one_token_per_level_is_top1():
+    """With K = 1 every level keeps one token, so ALLK (all kept tokens of each
+    level) and TOP1 (the rank-1 token) name the same key set: the coarse
+    tables and every output agree exactly."""
+    n, B, d = 4096, 16, 8
+    x = rng_inputs(n, d, seed=97)
+    a = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=1, rule="allk")
+    t = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=1)
+    np.testing.assert_array_equal(a["slices"][0]["sel"]["coarse"], t["slices"][0]["sel"]["coarse"])
+    for key in ("o", "lse", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[key], t[key])
+
+
+def test_allk_columns_and_key_set_size():
+    """ALLK: K_l columns per level; the level-1 columns of query block i are
+    its own fine selection (its level-1 ancestor is itself), and the key set
+    has K_1 B fine tokens plus sum_l K_l pooled ones."""
+    n, B, K, d = 4096, 16, 3, 8
+    x = rng_inputs(n, d, seed=98)
+    L = oracle.num_levels(n, B)
+    res = oracle.run(x["q"], x["k"], x["v"], B=B, K=K, backward=False, rule="allk")
+    sel = res["slices"][0]["sel"]
+    kl = oracle.level_topk(n, B, L, K)
+    assert list(sel["clev"]) == [l for l in range(1, L + 1) for _ in range(kl[l])]
+    np.testing.assert_array_equal(sel["coarse"][:, :kl[1]], sel["levels"][1])
+    _, _, nkeys = dense_masked(x["q"][0], x["k"][0], x["v"][0], B, L, L, sel["levels"][1], sel["coarse"],
+                               res["scale"], clev=sel["clev"])
+    assert nkeys == kl[1] * B + sum(kl[1:L + 1])
+
+
+@pytest.mark.parametrize("n,B,K,Le", [(1024, 16, 3, None), (512, 2, 2, 3), (4096, 16, 2, 1)])
+def test_allk_equals_dense_mask(n, B, K, Le):
+    d = 8
+    x = rng_inputs(n, d, seed=99)
+    L = oracle.num_levels(n, B)
+    Le = L if Le is None else Le
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=K, Le=Le, rule="allk")
+    s = res["slices"][0]
+    sel, coarse, clev = s["sel"]["levels"][1], s["sel"]["coarse"], s["sel"]["clev"]
+    o_ref, lse_ref, _ = dense_masked(x["q"][0], x["k"][0], x["v"][0], B, L, Le, sel, coarse, res["scale"], clev)
+    np.testing.assert_allclose(s["o"], o_ref, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(s["lse"], lse_ref, rtol=1e-12, atol=1e-12)
+    gq, gk, gv = _torch_masked_grads(x, B, L, Le, sel, coarse, res["scale"], clev)
+    np.testing.assert_allclose(s["dq"], gq, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s["dk"], gk, rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(s["dv"], gv, rtol=1e-9, atol=1e-11)
+
+
+def test_allk_sampled_rows_and_blocks_match_full():
+    """The row-subset forward and dq and the block-subset dk, dv (used for the
+    large GPU comparisons) agree with the whole-slice oracle under ALLK."""
+    n, B, K, d = 4096, 16, 3, 8
+    x = rng_inputs(n, d, seed=100)
+    L = oracle.num_levels(n, B)
+    res = oracle.run(x["q"], x["k"], x["v"], x["dout"], B=B, K=K, rule="allk")
+    s = res["slices"][0]
+    q, k, v, do = (x[a][0] for a in ("q", "k", "v", "dout"))
+    sel, coarse, clev, sc = s["sel"]["levels"][1], s["sel"]["coarse"], s["sel"]["clev"], res["scale"]
+    rows = np.array([0, 17, 300, 4095])
+    o_r, lse_r = oracle.fwd(q, k, v, s["kpyr"], s["vpyr"], B, L, L, sel, coarse, sc, qlist=rows, clev=clev)
+    np.testing.assert_array_equal(o_r, s["o"][rows])
+    dq_r = oracle.bwd_dq_rows(q, k, v, s["kpyr"], s["vpyr"], o_r, lse_r, do, B, L, L, sel, coarse, sc, rows,
+                              clev=clev)
+    np.testing.assert_allclose(dq_r, s["dq"][rows], rtol=1e-12, atol=1e-14)
+    blocks = np.array([0, 5, 255])
+    dk_b, dv_b = oracle.bwd_dkv_blocks(q, k, v, s["kpyr"], s["vpyr"], s["o"], s["lse"], do, B, L, L, sel, coarse,
+                                       sc, blocks, clev=clev)
+    fine = np.concatenate([np.arange(j * B, (j + 1) * B) for j in blocks])
+    np.testing.assert_allclose(dk_b, s["dk"][fine], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv_b, s["dv"][fine], rtol=1e-10, atol=1e-12)
 
 
 # ------------------------------------------------------- index reordering ---
