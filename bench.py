@@ -135,7 +135,7 @@ def work_model(w: synth.Workload, s) -> dict:
             "fwd": (4 * tok + bh * n * 4, 4 * d * pairs),
             # reads Q, dO, o, lse and the gathered K, V (each once from HBM);
             # writes dq, the (lse, D) pairs and the pooled-level partials
-            "bwd_dq": (6 * tok + bh * n * 12 + 2 * bh * s.n_blocks * s.enrich_levels * d * 4, 6 * d * pairs),
+            "bwd_dq": (6 * tok + bh * n * 12 + 2 * bh * s.n_blocks * s.enrich_cols * d * 4, 6 * d * pairs),
             "bwd_dkv": (6 * tok + bh * n * 8, 8 * d * fine_pairs),
             "transpose": (4 * bh * s.n_blocks * s.topk_level[1] * 3, 0),
             "select_level": (0, 2 * d * scored * bh),
@@ -473,7 +473,7 @@ def dense_comparator(w, dev, llsa_ms):
 
 # Throughput across the method's hyperparameters on the same inputs (the
 # pages' ablations vary K, B, L and L_e; only the step time is measured here):
-# (label, B, K, L (0: floor(log_B N - 1)), L_e (-1: all levels))
+# (label, B, K, L (0: floor(log_B N - 1)), L_e (-1: all levels)[, enrichment rule])
 SWEEP = [
     ("B16-K8", 16, 8, 0, -1),
     ("B16-K4", 16, 4, 0, -1),
@@ -487,6 +487,8 @@ SWEEP = [
     ("B16-K8-Le0", 16, 8, 0, 0),
     ("B16-K8-Le1", 16, 8, 0, 1),
     ("B16-K8-Le2", 16, 8, 0, 2),
+    ("B16-K8-ancestor", 16, 8, 0, -1, "ancestor"),
+    ("B16-K8-allk", 16, 8, 0, -1, "allk"),
 ]
 
 
@@ -507,8 +509,9 @@ def run_sweep(args):
     td = torch.bfloat16 if w0.dtype == "bf16" else torch.float32
     d = {k: torch.from_numpy(v).to(td).reshape(shape).to(dev) for k, v in x.items()}
     rows = []
-    for label, B, K, L, Le in SWEEP:
-        p = llsa.Params(w0.batch, w0.heads, w0.n, w0.d, block=B, topk=K, levels=L, enrich_levels=Le, dtype=w0.dtype)
+    for label, B, K, L, Le, *rule in SWEEP:
+        p = llsa.Params(w0.batch, w0.heads, w0.n, w0.d, block=B, topk=K, levels=L, enrich_levels=Le, dtype=w0.dtype,
+                        enrich_rule=rule[0] if rule else "top1")
         try:
             s = llsa.get_sizes(p)
             b = llsa.Buffers(p, dev)
@@ -540,7 +543,7 @@ def run_sweep(args):
         work = work_model(dataclasses.replace(w0, block=B, topk=K), s)
         tc = sorted(llsa_tensor_kernels(records))
         rows.append({"config": label, "block": B, "topk": K, "levels": s.levels, "enrich_levels": s.enrich_levels,
-                     "keys_per_query": s.keys_per_query, "ms_per_step": round(ms, 4),
+                     "enrich_rule": p.enrich_rule, "keys_per_query": s.keys_per_query, "ms_per_step": round(ms, 4),
                      "tflops": round(work["step_flops"] / (ms * 1e-3) / 1e12, 2),
                      "attention": "tensor cores (" + ", ".join(tc) + ")" if tc else "CUDA cores"})
         del b, dq, dk, dv

@@ -26,7 +26,8 @@ _lib = None
 LLSA_DTYPE_BF16, LLSA_DTYPE_F32 = 0, 1
 LLSA_ENRICH_TOP1 = 0
 LLSA_ENRICH_ANCESTOR = 1
-_RULES = {"top1": LLSA_ENRICH_TOP1, "ancestor": LLSA_ENRICH_ANCESTOR}
+LLSA_ENRICH_ALLK = 2
+_RULES = {"top1": LLSA_ENRICH_TOP1, "ancestor": LLSA_ENRICH_ANCESTOR, "allk": LLSA_ENRICH_ALLK}
 OP_POOL, OP_SELECT, OP_FWD, OP_TRANSPOSE, OP_BWD = range(5)
 MAX_LEVELS = 8
 
@@ -52,7 +53,8 @@ class _Sizes(ctypes.Structure):
                 ("row_offset", ctypes.c_int * (MAX_LEVELS + 1)), ("pyr_rows", ctypes.c_int),
                 ("n_blocks", ctypes.c_int), ("keys_per_query", ctypes.c_int), ("slices", ctypes.c_longlong),
                 ("level_idx_offset", ctypes.c_longlong * (MAX_LEVELS + 1)),
-                ("level_idx_per_slice", ctypes.c_longlong), ("scale", ctypes.c_float)]
+                ("level_idx_per_slice", ctypes.c_longlong), ("scale", ctypes.c_float),
+                ("coarse_cols", ctypes.c_int), ("enrich_cols", ctypes.c_int)]
 
 
 def lib_path() -> str:
@@ -111,7 +113,7 @@ class Params:
     enrich_levels: int = -1    # -1: all levels; 0: no enrichment
     dtype: str = "bf16"        # "bf16" or "fp32"
     scale: float = 0.0         # 0: 1/sqrt(d)
-    enrich_rule: str = "top1"  # "top1" or "ancestor"
+    enrich_rule: str = "top1"  # "top1", "ancestor" or "allk"
 
     def c(self) -> _Params:
         dt = {"bf16": LLSA_DTYPE_BF16, "fp32": LLSA_DTYPE_F32}.get(self.dtype)
@@ -119,7 +121,7 @@ class Params:
             raise ValueError(f"dtype must be 'bf16' or 'fp32', not {self.dtype!r}")
         rule = _RULES.get(self.enrich_rule)
         if rule is None:
-            raise ValueError(f"enrich_rule must be 'top1' or 'ancestor', not {self.enrich_rule!r}")
+            raise ValueError(f"enrich_rule must be 'top1', 'ancestor' or 'allk', not {self.enrich_rule!r}")
         return _Params(self.batch, self.heads, self.n, self.d, self.block, self.levels, self.topk,
                        self.enrich_levels, dt, self.scale, rule)
 
@@ -147,6 +149,8 @@ class Sizes:
     level_idx_offset: tuple
     level_idx_per_slice: int
     scale: float
+    coarse_cols: int   # entries per coarse_idx row (levels 1..L)
+    enrich_cols: int   # coarse keys per query (columns of levels 1..L_e)
 
 
 def get_sizes(p: Params) -> Sizes:
@@ -155,7 +159,7 @@ def get_sizes(p: Params) -> Sizes:
     L = s.levels
     return Sizes(L, s.enrich_levels, tuple(s.n_level[:L + 1]), tuple(s.topk_level[:L + 1]),
                  tuple(s.row_offset[:L + 1]), s.pyr_rows, s.n_blocks, s.keys_per_query, s.slices,
-                 tuple(s.level_idx_offset[:L + 1]), s.level_idx_per_slice, s.scale)
+                 tuple(s.level_idx_offset[:L + 1]), s.level_idx_per_slice, s.scale, s.coarse_cols, s.enrich_cols)
 
 
 def workspace_bytes(p: Params, op: int) -> int:
@@ -309,7 +313,7 @@ class Buffers:
         td = _tok_dtype(p)
         self.pyr = torch.empty((3, bh, s.pyr_rows, p.d), dtype=torch.float32, device=dev)
         self.sel_idx = torch.empty((bh, s.n_blocks, s.topk_level[1]), dtype=torch.int32, device=dev)
-        self.coarse_idx = torch.empty((bh, s.n_blocks, s.levels), dtype=torch.int32, device=dev)
+        self.coarse_idx = torch.empty((bh, s.n_blocks, s.coarse_cols), dtype=torch.int32, device=dev)
         self.level_idx = torch.empty((bh, max(1, s.level_idx_per_slice)), dtype=torch.int32, device=dev)
         self.o = torch.empty((p.batch, p.heads, p.n, p.d), dtype=td, device=dev)
         self.lse = torch.empty((p.batch, p.heads, p.n), dtype=torch.float32, device=dev)

@@ -113,7 +113,9 @@ static int derive(const llsa_params* p, Shape* s) {
     if (!p) return LLSA_ERR_INVALID_ARG;
     if (p->batch < 0 || p->heads < 0 || p->n < 1 || p->topk < 1) return LLSA_ERR_INVALID_ARG;
     if (p->dtype != LLSA_DTYPE_BF16 && p->dtype != LLSA_DTYPE_F32) return LLSA_ERR_DTYPE;
-    if (p->enrich_rule != LLSA_ENRICH_TOP1 && p->enrich_rule != LLSA_ENRICH_ANCESTOR) return LLSA_ERR_INVALID_ARG;
+    if (p->enrich_rule != LLSA_ENRICH_TOP1 && p->enrich_rule != LLSA_ENRICH_ANCESTOR &&
+        p->enrich_rule != LLSA_ENRICH_ALLK)
+        return LLSA_ERR_INVALID_ARG;
     if (!(p->scale >= 0.0f) || isinf(p->scale)) return LLSA_ERR_INVALID_ARG;
     if (p->d < 8 || p->d > 256 || p->d % 8 != 0) return LLSA_ERR_SHAPE;
     if (p->block < 2 || p->block > 1024) return LLSA_ERR_SHAPE;
@@ -153,6 +155,13 @@ static int derive(const llsa_params* p, Shape* s) {
     s->slices = (long long)p->batch * p->heads;
     s->n = p->n; s->d = p->d; s->B = p->block; s->L = L; s->Le = Le; s->rule = p->enrich_rule; s->topk = p->topk;
     s->K1 = s->topk_level[1]; s->T = s->n_level[1]; s->P = off; s->dtype = p->dtype;
+    // enrichment columns: one per level, or K_l per level under ALLK
+    s->col_off[1] = 0;
+    for (int l = 1; l <= L; l++)
+        s->col_off[l + 1] = s->col_off[l] + (p->enrich_rule == LLSA_ENRICH_ALLK ? s->topk_level[l] : 1);
+    s->C = s->col_off[L + 1];
+    s->Lc = s->col_off[Le + 1];
+    if (s->Lc > kMaxCoarse) return LLSA_ERR_UNSUPPORTED;
     s->scale = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
     if (s->slices * (long long)p->n * p->d > (1LL << 40)) return LLSA_ERR_UNSUPPORTED;
     return LLSA_OK;
@@ -191,7 +200,9 @@ int llsa_get_sizes(const llsa_params* p, llsa_sizes* out) {
     }
     out->pyr_rows = s.P;
     out->n_blocks = s.T;
-    out->keys_per_query = s.K1 * s.B + s.Le;
+    out->keys_per_query = s.K1 * s.B + s.Lc;
+    out->coarse_cols = s.C;
+    out->enrich_cols = s.Lc;
     out->slices = s.slices;
     out->level_idx_per_slice = s.level_idx_per_slice;
     out->scale = s.scale;

@@ -22,6 +22,12 @@ struct AttnArgs {
     LevelTable lv;
     int* status;
     int rule;  // enrichment rule
+    // enrichment columns: C per coarse row, Lc used (levels 1..Le); column c
+    // holds a token of level col_level[c]; level l owns columns
+    // col_off[l] .. col_off[l+1]-1
+    int C, Lc;
+    unsigned char col_level[kMaxCoarse];
+    short col_off[LLSA_MAX_LEVELS + 2];
 };
 
 AttnArgs make_attn_args(const Shape& s);

@@ -131,7 +131,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             const long long g = blockIdx.x + bl * G;
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
-            if (role == 0) return lane < Le ? a.coarse[(slice * a.T + i) * a.L + lane] : 0;
+            if (role == 0) return lane < Le ? a.coarse[(slice * a.T + i) * a.C + lane] : 0;
             return lane < K1 ? a.sel[(slice * a.T + i) * a.K1 + lane] : 0;
         };
         const uint32_t my_bytes = role == 0 ? 3 * C::Q_BYTES + 64 + 2 * Le * D * 4 : C::KV_BYTES;

@@ -140,7 +140,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
             if (lane < K1) jb = a.sel[(slice * a.T + i) * a.K1 + lane];
-            if (lane < Le) ce = a.coarse[(slice * a.T + i) * a.L + lane];
+            if (lane < Le) ce = a.coarse[(slice * a.T + i) * a.C + lane];
         };
         int jb0, ce0, jb1, ce1;
         load_idx(pw, jb0, ce0);
@@ -555,7 +555,7 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
             if (role < 2) return lane < K1 ? a.sel[(slice * a.T + i) * a.K1 + lane] : 0;
-            return lane < Le ? a.coarse[(slice * a.T + i) * a.L + lane] : 0;
+            return lane < Le ? a.coarse[(slice * a.T + i) * a.C + lane] : 0;
         };
         const uint32_t my_bytes = role == 0 ? C::Q_BYTES + C::KV_BYTES : role == 1 ? C::KV_BYTES : 2 * Le * D * 4;
         int ix0 = load_idx(0), ix1 = load_idx(1);
@@ -962,8 +962,9 @@ int launch_any(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const C
 }  // namespace
 
 bool fwd_tc_supported(const Shape& s) {
+    // one enrichment column per level (the pooled keys sit in four row slots)
     return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && (s.d == 64 || s.d == 128) && (s.K1 == 8 || s.K1 == 16) &&
-           s.Le <= 4 && s.slices * (long long)s.n < (1LL << 31);
+           s.Le <= 4 && s.Lc == s.Le && s.slices * (long long)s.n < (1LL << 31);
 }
 
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {

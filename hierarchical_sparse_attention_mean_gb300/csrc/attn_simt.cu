@@ -97,16 +97,17 @@ __device__ __forceinline__ void key_tokens(const AttnArgs& a, long long slice, i
 }
 
 __device__ __forceinline__ const float* coarse_row(const AttnArgs& a, const float* pyr, long long slice, int i,
-                                                   int l) {
-    // level l+1 enrichment token of query block i
-    const int e = checked(a.coarse[(slice * a.T + i) * a.L + l], a.lv.n_level[l + 1], a.status);
-    return pyr + slice * a.pyr_stride + (long long)(a.lv.row_offset[l + 1] + e) * a.d;
+                                                   int c) {
+    // the enrichment token in column c of query block i (level col_level[c])
+    const int l = a.col_level[c];
+    const int e = checked(a.coarse[(slice * a.T + i) * a.C + c], a.lv.n_level[l], a.status);
+    return pyr + slice * a.pyr_stride + (long long)(a.lv.row_offset[l] + e) * a.d;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(512) fwd_simt_kernel(AttnArgs a) {
     extern __shared__ float4 sm4[];
-    const int d = a.d, B = a.B, nf = a.K1 * B, NK = nf + a.Le, NKP = NK | 1, ds = d + 4;
+    const int d = a.d, B = a.B, nf = a.K1 * B, NK = nf + a.Lc, NKP = NK | 1, ds = d + 4;
     float* qs = reinterpret_cast<float*>(sm4);
     float* kv = qs + B * ds;
     float* S = kv + kTileKeys * ds;
@@ -130,10 +131,10 @@ __global__ void __launch_bounds__(512) fwd_simt_kernel(AttnArgs a) {
                 S[r * NKP + t0 + kk] = a.scale * dot_smem(qs + r * ds, kv + kk * ds, d);
         __syncthreads();
     }
-    for (int pr = tid; pr < B * a.Le; pr += nt) {
-        const int r = pr / a.Le, l = pr % a.Le;
-        S[r * NKP + nf + l] = a.scale * dot_smem_global(qs + r * ds, coarse_row(a, a.kpyr, slice, i, l), d) +
-                              (float)(l + 1) * a.lnB;
+    for (int pr = tid; pr < B * a.Lc; pr += nt) {
+        const int r = pr / a.Lc, c = pr % a.Lc;
+        S[r * NKP + nf + c] = a.scale * dot_smem_global(qs + r * ds, coarse_row(a, a.kpyr, slice, i, c), d) +
+                              (float)a.col_level[c] * a.lnB;
     }
     __syncthreads();
     const int warp = tid >> 5, lane = tid & 31;
@@ -181,9 +182,9 @@ __global__ void __launch_bounds__(512) fwd_simt_kernel(AttnArgs a) {
         const int it = tid + m * nt;
         if (it < items) {
             const int r = it / C4, c4 = it % C4;
-            for (int l = 0; l < a.Le; l++) {
-                const float p = S[r * NKP + nf + l];
-                const float4 v4 = __ldg(reinterpret_cast<const float4*>(coarse_row(a, a.vpyr, slice, i, l) + c4 * 4));
+            for (int c = 0; c < a.Lc; c++) {
+                const float p = S[r * NKP + nf + c];
+                const float4 v4 = __ldg(reinterpret_cast<const float4*>(coarse_row(a, a.vpyr, slice, i, c) + c4 * 4));
                 acc[m][0] = fmaf(p, v4.x, acc[m][0]); acc[m][1] = fmaf(p, v4.y, acc[m][1]);
                 acc[m][2] = fmaf(p, v4.z, acc[m][2]); acc[m][3] = fmaf(p, v4.w, acc[m][3]);
             }
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__(512) fwd_simt_kernel(AttnArgs a) {
 template <typename T>
 __global__ void __launch_bounds__(512) bwd_dq_simt_kernel(AttnArgs a) {
     extern __shared__ float4 sm4[];
-    const int d = a.d, B = a.B, nf = a.K1 * B, NK = nf + a.Le, NKP = NK | 1, ds = d + 4;
+    const int d = a.d, B = a.B, nf = a.K1 * B, NK = nf + a.Lc, NKP = NK | 1, ds = d + 4;
     float* qs = reinterpret_cast<float*>(sm4);
     float* dos = qs + B * ds;
     float* ks = dos + B * ds;
@@ -250,14 +251,14 @@ __global__ void __launch_bounds__(512) bwd_dq_simt_kernel(AttnArgs a) {
             }
         __syncthreads();
     }
-    for (int pr = tid; pr < B * a.Le; pr += nt) {
-        const int r = pr / a.Le, l = pr % a.Le;
-        const float s = a.scale * dot_smem_global(qs + r * ds, coarse_row(a, a.kpyr, slice, i, l), d) +
-                        (float)(l + 1) * a.lnB;
+    for (int pr = tid; pr < B * a.Lc; pr += nt) {
+        const int r = pr / a.Lc, c = pr % a.Lc;
+        const float s = a.scale * dot_smem_global(qs + r * ds, coarse_row(a, a.kpyr, slice, i, c), d) +
+                        (float)a.col_level[c] * a.lnB;
         const float p = expf(s - lse_s[r]);
-        const float dp = dot_smem_global(dos + r * ds, coarse_row(a, a.vpyr, slice, i, l), d);
-        P[r * NKP + nf + l] = p;
-        dS[r * NKP + nf + l] = p * (dp - D_s[r]);
+        const float dp = dot_smem_global(dos + r * ds, coarse_row(a, a.vpyr, slice, i, c), d);
+        P[r * NKP + nf + c] = p;
+        dS[r * NKP + nf + c] = p * (dp - D_s[r]);
     }
     __syncthreads();
     // dq = scale * sum_x dS_x k_x
@@ -292,9 +293,9 @@ __global__ void __launch_bounds__(512) bwd_dq_simt_kernel(AttnArgs a) {
         const int it = tid + m * nt;
         if (it < items) {
             const int r = it / C4, c4 = it % C4;
-            for (int l = 0; l < a.Le; l++) {
-                const float g = dS[r * NKP + nf + l];
-                const float4 k4 = __ldg(reinterpret_cast<const float4*>(coarse_row(a, a.kpyr, slice, i, l) + c4 * 4));
+            for (int c = 0; c < a.Lc; c++) {
+                const float g = dS[r * NKP + nf + c];
+                const float4 k4 = __ldg(reinterpret_cast<const float4*>(coarse_row(a, a.kpyr, slice, i, c) + c4 * 4));
                 acc[m][0] = fmaf(g, k4.x, acc[m][0]); acc[m][1] = fmaf(g, k4.y, acc[m][1]);
                 acc[m][2] = fmaf(g, k4.z, acc[m][2]); acc[m][3] = fmaf(g, k4.w, acc[m][3]);
             }
@@ -303,8 +304,8 @@ __global__ void __launch_bounds__(512) bwd_dq_simt_kernel(AttnArgs a) {
         }
     }
     // coarse partials of this query block: gK = scale sum_t dS_t q_t,
-    // gV = sum_t P_t dO_t, per enrichment level
-    for (int it = tid; it < a.Le * C4; it += nt) {
+    // gV = sum_t P_t dO_t, per enrichment column
+    for (int it = tid; it < a.Lc * C4; it += nt) {
         const int l = it / C4, c4 = it % C4;
         float gk[4] = {0.f, 0.f, 0.f, 0.f}, gv[4] = {0.f, 0.f, 0.f, 0.f};
         for (int r = 0; r < B; r++) {
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(512) bwd_dq_simt_kernel(AttnArgs a) {
             gv[0] = fmaf(p, o4.x, gv[0]); gv[1] = fmaf(p, o4.y, gv[1]);
             gv[2] = fmaf(p, o4.z, gv[2]); gv[3] = fmaf(p, o4.w, gv[3]);
         }
-        const long long off = ((slice * a.T + i) * a.Le + l) * (long long)d + c4 * 4;
+        const long long off = ((slice * a.T + i) * a.Lc + l) * (long long)d + c4 * 4;
         *reinterpret_cast<float4*>(a.gK + off) =
             make_float4(a.scale * gk[0], a.scale * gk[1], a.scale * gk[2], a.scale * gk[3]);
         *reinterpret_cast<float4*>(a.gV + off) = make_float4(gv[0], gv[1], gv[2], gv[3]);
@@ -446,7 +447,7 @@ __device__ __forceinline__ void load_cols(const float* p, bool ok, float (&v)[kC
 }
 
 template <int kCols>  // columns per lane: d <= 32 * kCols, d % kCols == 0
-__global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(AttnArgs a, int rows) {
+__global__ void __launch_bounds__(32 * kReduceWarps, kCols >= 8 ? 4 : 6) coarse_reduce_kernel(AttnArgs a, int rows) {
     constexpr int kUnroll = kCols >= 4 ? 2 : 4;  // rows in flight (spans are pre-summed: few rows per token)
     __shared__ int hits[kReduceWarps][32];
     const long long slice = blockIdx.y;
@@ -460,10 +461,11 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(Att
     const int e = row - a.lv.row_offset[l];
     const int d = a.d;
     const bool active = lane * kCols < d;
-    const long long rstride = (long long)a.Le * d;  // between consecutive query blocks
-    const long long base = (slice * a.T * a.Le + (l - 1)) * (long long)d + lane * kCols;
+    // partial rows [T][Lc]: row x = query block * Lc + enrichment column
+    const long long base = slice * a.T * (long long)a.Lc * d + lane * kCols;
     const float* gk = a.gK + base;
     const float* gv = a.gV + base;
+    const int c0 = a.col_off[l], c1 = a.col_off[l + 1];  // the columns of level l
     float ak[kCols], av[kCols];
 #pragma unroll
     for (int c = 0; c < kCols; c++) ak[c] = av[c] = 0.f;
@@ -474,7 +476,7 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(Att
 #pragma unroll
             for (int u = 0; u < kUnroll; u++) {
                 const bool ok = active && r0 + u < count;
-                const long long off = ok ? (long long)src(r0 + u) * rstride : 0;
+                const long long off = ok ? (long long)src(r0 + u) * d : 0;
                 load_cols<kCols>(gk + off, ok, pk[u]);
                 load_cols<kCols>(gv + off, ok, pv[u]);
             }
@@ -487,20 +489,27 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(Att
                 }
         }
     };
+    // a hit is a partial row x = block * Lc + column whose token is e (the
+    // columns of one level hold distinct tokens, so at most one per block)
     int* h = hits[warp];
     if (l == 1 && a.rule == LLSA_ENRICH_ANCESTOR) {
         // the level-1 token e is block e's own pooled keys: used by block e only
-        add_rows(1, [&](int) { return e; });
+        add_rows(1, [&](int) { return e * a.Lc + c0; });
     } else if (l == 1) {
+        // level-1 tokens are selected blocks: the candidates are column e of the CSC
         const int* cp = a.col_ptr + slice * (long long)(a.T + 1);
         const int* ri = a.row_idx + slice * (long long)a.T * a.K1;
         const int beg = cp[e], end = cp[e + 1];
         for (int x0 = beg; x0 < end; x0 += 32) {
             const int x = x0 + lane;
             const int i = x < end ? ri[x] : -1;
-            const bool hit = i >= 0 && i < a.T && a.coarse[(slice * a.T + i) * a.L] == e;
+            int col = -1;
+            if (i >= 0 && i < a.T)
+                for (int c = c0; c < c1; c++)
+                    if (a.coarse[(slice * a.T + i) * a.C + c] == e) col = c;
+            const bool hit = col >= 0;
             const unsigned bits = __ballot_sync(0xffffffffu, hit);
-            if (hit) h[__popc(bits & ((1u << lane) - 1u))] = i;
+            if (hit) h[__popc(bits & ((1u << lane) - 1u))] = i * a.Lc + col;
             __syncwarp();
             add_rows(__popc(bits), [&](int r) { return h[r]; });
             __syncwarp();
@@ -511,12 +520,16 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(Att
         const int nl = a.lv.n_level[l];
         for (int a0 = 0; a0 < nl; a0 += 32) {
             const int anc = a0 + lane;
-            const bool hit = anc < nl && a.coarse[(slice * a.T + (long long)anc * span) * a.L + (l - 1)] == e;
+            int col = -1;
+            if (anc < nl)
+                for (int c = c0; c < c1; c++)
+                    if (a.coarse[(slice * a.T + (long long)anc * span) * a.C + c] == e) col = c;
+            const bool hit = col >= 0;
             const unsigned bits = __ballot_sync(0xffffffffu, hit);
-            if (hit) h[__popc(bits & ((1u << lane) - 1u))] = anc;
-            __syncwarp();
             // ancestor anc's span sum sits in the row of block anc * span
-            add_rows(__popc(bits), [&](int r) { return h[r] * span; });
+            if (hit) h[__popc(bits & ((1u << lane) - 1u))] = anc * span * a.Lc + col;
+            __syncwarp();
+            add_rows(__popc(bits), [&](int r) { return h[r]; });
             __syncwarp();
         }
     }
@@ -531,21 +544,23 @@ __global__ void __launch_bounds__(32 * kReduceWarps, 6) coarse_reduce_kernel(Att
 }
 
 // Pooled levels l >= 2: the query blocks under one level-l ancestor share its
-// token, so their partials are first summed per ancestor. Step `step` folds,
-// for every level l > step, each group of B consecutive rows at stride
-// B^(step-1) into the group's first row, in place and in ascending order;
-// after steps 1..l-1 the row of block anc * B^(l-1) holds ancestor anc's sum.
+// tokens, so their partials are first summed per ancestor. Step `step` folds,
+// for every enrichment column of a level l > step, each group of B
+// consecutive rows at stride B^(step-1) into the group's first row, in place
+// and in ascending order; after steps 1..l-1 the row of block anc * B^(l-1)
+// holds ancestor anc's sum.
 template <int kCols>
 __global__ void __launch_bounds__(32 * kReduceWarps) coarse_span_kernel(AttnArgs a, int step, int stride, int groups) {
     const long long slice = blockIdx.y;
     const int lane = threadIdx.x & 31;
     const int id = (int)(blockIdx.x * kReduceWarps + (threadIdx.x >> 5));
-    if (id >= (a.Le - step) * groups) return;
-    const int l = step + 1 + id / groups, grp = id % groups;
+    const int cfirst = a.col_off[step + 1];  // the first column of level step + 1
+    if (id >= (a.Lc - cfirst) * groups) return;
+    const int col = cfirst + id / groups, grp = id % groups;
     const int d = a.d;
     const bool active = lane * kCols < d;
-    const long long rstride = (long long)a.Le * d;
-    const long long base = (slice * a.T * a.Le + (l - 1)) * (long long)d + lane * kCols;
+    const long long rstride = (long long)a.Lc * d;
+    const long long base = (slice * a.T * a.Lc + col) * (long long)d + lane * kCols;
     const long long first = (long long)grp * a.B * stride;
     float ak[kCols], av[kCols];
 #pragma unroll
@@ -589,6 +604,11 @@ AttnArgs make_attn_args(const Shape& s) {
     a.lv = level_table(s);
     a.status = status_ptr();
     a.rule = s.rule;
+    a.C = s.C;
+    a.Lc = s.Lc;
+    for (int l = 1; l <= s.L + 1 && l <= LLSA_MAX_LEVELS + 1; l++) a.col_off[l] = (short)s.col_off[l];
+    for (int l = 1; l <= s.Le; l++)
+        for (int c = s.col_off[l]; c < s.col_off[l + 1] && c < kMaxCoarse; c++) a.col_level[c] = (unsigned char)l;
     return a;
 }
 
@@ -596,7 +616,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 size_t bwd_workspace_bytes(const Shape& s) {
     size_t b = align256(2 * sizeof(float) * s.slices * (size_t)s.n);                   // D (or (lse, D) pairs)
-    b += 2 * align256(sizeof(float) * s.slices * (size_t)s.T * s.Le * s.d);            // gK, gV
+    b += 2 * align256(sizeof(float) * s.slices * (size_t)s.T * s.Lc * s.d);            // gK, gV
     b += 2 * align256(sizeof(float) * s.slices * (size_t)s.P * s.d);                   // dKc, dVc
     return b;
 }
@@ -605,7 +625,7 @@ void carve_bwd_workspace(const Shape& s, void* ws, AttnArgs* a) {
     char* w = static_cast<char*>(ws);
     a->Dbuf = reinterpret_cast<float*>(w);
     w += align256(2 * sizeof(float) * s.slices * (size_t)s.n);
-    const size_t gsz = align256(sizeof(float) * s.slices * (size_t)s.T * s.Le * s.d);
+    const size_t gsz = align256(sizeof(float) * s.slices * (size_t)s.T * s.Lc * s.d);
     a->gK = reinterpret_cast<float*>(w); w += gsz;
     a->gV = reinterpret_cast<float*>(w); w += gsz;
     const size_t csz = align256(sizeof(float) * s.slices * (size_t)s.P * s.d);
@@ -618,7 +638,7 @@ int launch_spans(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     int stride = 1, groups = s.T;
     for (int step = 1; step < s.Le; step++) {
         groups /= s.B;
-        const int warps = (s.Le - step) * groups;
+        const int warps = (s.Lc - s.col_off[step + 1]) * groups;
         const dim3 grid((warps + kReduceWarps - 1) / kReduceWarps, (unsigned)s.slices);
         LLSA_LAUNCH("coarse_reduce", st, coarse_span_kernel<kCols><<<grid, 32 * kReduceWarps, 0, st>>>(a, step, stride, groups));
         stride *= s.B;
@@ -650,7 +670,7 @@ int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st) {
 int launch_fwd_simt(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     const int nt = attn_threads(s.B, s.d);
     if (nt < 0 || s.slices > 65535) return LLSA_ERR_UNSUPPORTED;
-    const int ds = s.d + 4, NKP = (s.K1 * s.B + s.Le) | 1;
+    const int ds = s.d + 4, NKP = (s.K1 * s.B + s.Lc) | 1;
     const size_t smem = sizeof(float) * ((size_t)s.B * ds + kTileKeys * ds + (size_t)s.B * NKP) +
                         sizeof(int) * (size_t)s.K1 * s.B;
     if (smem > 220 * 1024) return LLSA_ERR_UNSUPPORTED;
@@ -668,7 +688,7 @@ int launch_fwd_simt(const Shape& s, const AttnArgs& a, cudaStream_t st) {
 int launch_bwd_dq_simt(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     const int nt = attn_threads(s.B, s.d);
     if (nt < 0 || s.slices > 65535) return LLSA_ERR_UNSUPPORTED;
-    const int ds = s.d + 4, NKP = (s.K1 * s.B + s.Le) | 1;
+    const int ds = s.d + 4, NKP = (s.K1 * s.B + s.Lc) | 1;
     const size_t smem = sizeof(float) * (2 * (size_t)s.B * ds + 2 * kTileKeys * ds + 2 * (size_t)s.B * NKP +
                                          2 * (size_t)s.B) + sizeof(int) * (size_t)s.K1 * s.B;
     if (smem > 220 * 1024) return LLSA_ERR_UNSUPPORTED;

@@ -20,12 +20,18 @@ struct Shape {
     float scale;
     int rule;  // enrichment rule (LLSA_ENRICH_*)
     int topk;  // K as requested (before the per-level clamp)
+    // enrichment columns: C per coarse_idx row (levels 1..L), Lc of them used
+    // (levels 1..L_e, a prefix); level l owns columns col_off[l] .. col_off[l+1]-1
+    int C, Lc;
+    int col_off[LLSA_MAX_LEVELS + 2];
     int n_level[LLSA_MAX_LEVELS + 1];
     int topk_level[LLSA_MAX_LEVELS + 1];
     int row_offset[LLSA_MAX_LEVELS + 1];
     long long level_idx_offset[LLSA_MAX_LEVELS + 1];
     long long level_idx_per_slice;
 };
+
+constexpr int kMaxCoarse = 64;  // coarse keys per query (ALLK)
 
 // Level tables passed by value to kernels.
 struct LevelTable {

@@ -43,8 +43,9 @@ struct SelectArgs {
     int Kl;
     int* out;
     long long out_stride;
-    int* coarse;           // [slices][T][L]
-    int T, L, level, span; // span = B^(level-1)
+    int* coarse;           // [slices][T][ccols]
+    int T, ccols, col0;    // coarse row length; this level's first column
+    int level, span;       // span = B^(level-1)
     int rows_per_cta;
     int C;                 // candidates per row
     int n_parent;          // rows of the parent level (index check)
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? (DT > 0 ? 3 : 4) : 1
     float* scores = qrows + kMaxRows * d;                            // [rows][C]
     int* cand = reinterpret_cast<int*>(scores + kMaxRows * C);       // [C]
     int* kept = cand + C;                                            // [rows][kMaxKeep]
+    int* sorted = kept + kMaxRows * kMaxKeep;                        // [rows][kMaxKeep]
 
     const long long slice = blockIdx.y;
     const int row0 = blockIdx.x * a.rows_per_cta;
@@ -198,23 +200,32 @@ __global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? (DT > 0 ? 3 : 4) : 1
     __syncwarp();
     const int row = row0 + warp;
     int* orow = a.out + slice * a.out_stride + (long long)row * a.Kl;
+    int* srow = sorted + warp * kMaxKeep;
     for (int k = lane; k < a.Kl; k += 32) {
         const int v = krow[k];
         int rank = 0;
         for (int k2 = 0; k2 < a.Kl; k2++) rank += krow[k2] < v;
         orow[rank] = v;
+        srow[rank] = v;
     }
-    // enrichment index: every level-1 descendant of this row gets the row's
-    // rank-1 selection (TOP1) or the row itself (ANCESTOR)
-    const int top1 = a.rule == LLSA_ENRICH_ANCESTOR ? row : krow[0];
-    int* crow = a.coarse + (slice * a.T + (long long)row * a.span) * a.L + (a.level - 1);
-    for (int q = lane; q < a.span; q += 32) crow[(long long)q * a.L] = top1;
+    __syncwarp();
+    // enrichment index: every level-1 descendant of this row gets, in this
+    // level's columns, the row's rank-1 selection (TOP1), the row itself
+    // (ANCESTOR) or the whole ascending row (ALLK)
+    int* crow = a.coarse + (slice * a.T + (long long)row * a.span) * a.ccols + a.col0;
+    if (a.rule == LLSA_ENRICH_ALLK) {
+        for (int x = lane; x < a.span * a.Kl; x += 32)
+            crow[(long long)(x / a.Kl) * a.ccols + x % a.Kl] = srow[x % a.Kl];
+    } else {
+        const int top1 = a.rule == LLSA_ENRICH_ANCESTOR ? row : krow[0];
+        for (int q = lane; q < a.span; q += 32) crow[(long long)q * a.ccols] = top1;
+    }
 }
 
 template <int KPL>
 size_t level_smem(const SelectArgs& a) {
     return sizeof(float) * (32 * KPL * (a.d + 4) + kMaxRows * a.d + kMaxRows * a.C) +
-           sizeof(int) * (a.C + kMaxRows * kMaxKeep);
+           sizeof(int) * (a.C + 2 * kMaxRows * kMaxKeep);
 }
 
 template <int CPL, int KPL, int DT>
@@ -267,7 +278,8 @@ int launch_select(const Shape& s, const float* pyr, int32_t* sel_idx, int32_t* c
         a.Kl = s.topk_level[l];
         a.coarse = coarse_idx;
         a.T = s.T;
-        a.L = s.L;
+        a.ccols = s.C;
+        a.col0 = s.col_off[l];
         a.level = l;
         a.span = (int)span;
         a.status = status_ptr();

@@ -56,14 +56,16 @@ enum {
 
 enum { LLSA_DTYPE_BF16 = 0, LLSA_DTYPE_F32 = 1 };
 
-/* Enrichment rule: which coarse token of level l joins query block i's keys
+/* Enrichment rule: which coarse tokens of level l join query block i's keys
  * ("Core claim": one coarse token from every level; the page does not say
- * which, so both readings are offered).
+ * which, so three readings are offered).
  * TOP1: the rank-1 selection of level l for i's level-l ancestor
  *       floor(i / B^(l-1));
  * ANCESTOR: that ancestor itself, the level-l token whose B^l tokens contain
- *       query block i. */
-enum { LLSA_ENRICH_TOP1 = 0, LLSA_ENRICH_ANCESTOR = 1 };
+ *       query block i;
+ * ALLK: all K_l selections of level l for that ancestor (K_l tokens per
+ *       level instead of one, each with weight B^l). */
+enum { LLSA_ENRICH_TOP1 = 0, LLSA_ENRICH_ANCESTOR = 1, LLSA_ENRICH_ALLK = 2 };
 
 enum { LLSA_OP_POOL = 0, LLSA_OP_SELECT = 1, LLSA_OP_FWD = 2, LLSA_OP_TRANSPOSE = 3, LLSA_OP_BWD = 4 };
 
@@ -77,7 +79,7 @@ typedef struct llsa_params {
     int enrich_levels;  /* L_e; -1 selects L; 0 disables enrichment */
     int dtype;          /* LLSA_DTYPE_BF16 or LLSA_DTYPE_F32 */
     float scale;        /* softmax scale; 0 selects 1/sqrt(d) */
-    int enrich_rule;    /* LLSA_ENRICH_TOP1 or LLSA_ENRICH_ANCESTOR */
+    int enrich_rule;    /* LLSA_ENRICH_TOP1, LLSA_ENRICH_ANCESTOR or LLSA_ENRICH_ALLK */
 } llsa_params;
 
 /* Sizes derived from the parameters. */
@@ -89,11 +91,13 @@ typedef struct llsa_sizes {
     int row_offset[LLSA_MAX_LEVELS + 1];      /* first pyramid row of level l (index 0 unused) */
     int pyr_rows;                             /* P */
     int n_blocks;                             /* T = n_1 */
-    int keys_per_query;                       /* K_1 * B + L_e */
+    int keys_per_query;                       /* K_1 * B + enrich_cols */
     long long slices;                         /* batch * heads */
     long long level_idx_offset[LLSA_MAX_LEVELS + 1]; /* int32 offset of level l >= 2 inside one slice of level_idx */
     long long level_idx_per_slice;            /* int32 entries per slice of level_idx */
     float scale;                              /* effective softmax scale */
+    int coarse_cols;                          /* C: entries per row of coarse_idx (levels 1..L) */
+    int enrich_cols;                          /* coarse keys per query: the columns of levels 1..L_e */
 } llsa_sizes;
 
 /* Derive sizes and validate the parameters (no device work). */
@@ -119,24 +123,28 @@ int llsa_pool(const llsa_params *p, const void *q, const void *k, const void *v,
  * of pooled Q and pooled K in fp32; ties go to the lower index.
  *   pyr        : input from llsa_pool.
  *   sel_idx    : output int32 [batch*heads][T][K_1], I^(1), rows ascending.
- *   coarse_idx : output int32 [batch*heads][T][L]; entry (i, l-1) is the level-l
- *                enrichment token of query block i (rule p->enrich_rule).
+ *   coarse_idx : output int32 [batch*heads][T][C] (C = coarse_cols): the
+ *                enrichment tokens of query block i, level 1 first; one
+ *                column per level (TOP1, ANCESTOR), or K_l columns holding
+ *                I^(l)[floor(i / B^(l-1))] ascending (ALLK).
  *   level_idx  : output int32, I^(2) .. I^(L), each slice holding
  *                level_idx_per_slice entries, level l at level_idx_offset[l]
  *                as n_l rows of K_l ascending indices. May be NULL when L == 1.
- * Limits: at most 1024 candidates per query token at any level. */
+ * Limits: at most 1024 candidates per query token at any level; ALLK at most
+ * 64 coarse keys per query (enrich_cols). */
 int llsa_select(const llsa_params *p, const float *pyr, int32_t *sel_idx, int32_t *coarse_idx,
                 int32_t *level_idx, void *ws, size_t ws_bytes, void *stream);
 
 /* Block-sparse attention with hierarchical KV enrichment ("Core claim").
  * For token t of query block i, the keys are the B tokens of each block in
- * sel_idx[i] plus, for l = 1..L_e, the pooled token K^(l)[coarse_idx[i][l-1]]
- * with weight B^l (logit + ln B^l, KV Reweighting); then
+ * sel_idx[i] plus, for each column c of coarse_idx[i] whose level l is at most
+ * L_e, the pooled token K^(l)[coarse_idx[i][c]] with weight B^l (logit +
+ * ln B^l, KV Reweighting); then
  *   lse_t = ln sum_x exp(s_tx),  o_t = sum_x exp(s_tx - lse_t) v_x,
  * with s_tx = scale * q_t . k_x (+ ln B^l for coarse keys).
  *   q, k, v    : [batch, heads, N, d] (p->dtype); pyr from llsa_pool.
  *   sel_idx    : int32 [batch*heads][T][K_1], entries in [0, T).
- *   coarse_idx : int32 [batch*heads][T][L], level-l entries in [0, n_l).
+ *   coarse_idx : int32 [batch*heads][T][C], level-l entries in [0, n_l).
  *   o          : output [batch, heads, N, d] (p->dtype).
  *   lse        : output fp32 [batch, heads, N] (natural log). */
 int llsa_fwd(const llsa_params *p, const void *q, const void *k, const void *v, const float *pyr,

@@ -84,13 +84,25 @@ def test_invalid_parameters_rejected_on_host(lib, kw, code):
 
 def test_enrichment_rules(lib):
     for rule in ("top1", "ancestor"):
-        assert llsa.get_sizes(llsa.Params(1, 1, 4096, 64, enrich_rule=rule)).keys_per_query == 8 * 16 + 2
+        s = llsa.get_sizes(llsa.Params(1, 1, 4096, 64, enrich_rule=rule))
+        assert (s.keys_per_query, s.coarse_cols, s.enrich_cols) == (8 * 16 + 2, 2, 2)
+    # ALLK: K_l columns per level (N = 4096, B = 16: n_2 = 16 tokens, K_2 = 8)
+    s = llsa.get_sizes(llsa.Params(1, 1, 4096, 64, enrich_rule="allk"))
+    assert (s.keys_per_query, s.coarse_cols, s.enrich_cols) == (8 * 16 + 16, 16, 16)
+    s = llsa.get_sizes(llsa.Params(1, 1, 4096, 64, enrich_rule="allk", enrich_levels=1))
+    assert (s.keys_per_query, s.coarse_cols, s.enrich_cols) == (8 * 16 + 8, 16, 8)
+    # the coarsest level clamps K to its tokens: K = 32 keeps 16 at level 2
+    s = llsa.get_sizes(llsa.Params(1, 1, 4096, 64, topk=32, enrich_rule="allk"))
+    assert (s.coarse_cols, s.enrich_cols) == (48, 48)
+    # more than 64 coarse keys per query is beyond the kernels
+    with pytest.raises(llsa.LLSAError):
+        llsa.get_sizes(llsa.Params(1, 1, 65536, 64, topk=32, enrich_rule="allk"))
     p = llsa.Params(1, 1, 4096, 64).c()
-    p.enrich_rule = 2  # no such rule
+    p.enrich_rule = 3  # no such rule
     s = llsa._Sizes()
     assert lib.llsa_get_sizes(ctypes.byref(p), ctypes.byref(s)) == -1
     with pytest.raises(ValueError):
-        llsa.Params(1, 1, 4096, 64, enrich_rule="allk").c()
+        llsa.Params(1, 1, 4096, 64, enrich_rule="all").c()
 
 
 def test_bad_dtype_and_empty_input(lib):

@@ -289,3 +289,34 @@ def test_ancestor_rule_end_to_end(name):
             np.testing.assert_array_equal(out["gpu_coarse"][s][:, l - 1], np.arange(T) // w.block ** (l - 1))
     excluded = compare_end_to_end(w, ref, out)
     assert excluded <= max(1, 0.01 * w.bh * (w.n // w.block))
+
+
+@pytest.mark.parametrize("name,Le", [("ragged-h3", None), ("ragged-h3", 1), ("B4-L4-fp32", None),
+                                     ("d128-K16", None), ("n4096-bf16", None)])
+def test_allk_rule(name, Le):
+    """ALLK enrichment (every token a level keeps for the block's ancestor):
+    the selection equals TOP1's; the enrichment table holds, for each level,
+    the GPU's own ascending row of the ancestor; on the oracle's indices the
+    outputs and gradients match the oracle."""
+    w = CASES[name]
+    x = synth.make_inputs(w)
+    kw = {} if Le is None else {"enrich_levels": Le}
+    p = params_of(w, enrich_rule="allk", **kw)
+    out, _ = gpu_stage_outputs(w, x, p=p, backward=False)
+    top1, _ = gpu_stage_outputs(w, x, p=params_of(w, **kw), backward=False)
+    L = len(out["gpu_levels"]) - 1
+    clev = oracle.coarse_levels(w.n, w.block, L, w.topk, "allk")
+    T = w.n // w.block
+    for l in range(1, L + 1):
+        np.testing.assert_array_equal(out["gpu_levels"][l], top1["gpu_levels"][l])
+        cols = np.nonzero(clev == l)[0]
+        anc = np.arange(T) // w.block ** (l - 1)
+        for s in range(w.bh):
+            np.testing.assert_array_equal(out["gpu_coarse"][s][:, cols], out["gpu_levels"][l][s][anc])
+    ref = run_oracle(w, x, rule="allk", **({} if Le is None else {"Le": Le}))
+    got, _ = gpu_stage_outputs(w, x, p=p, backward=w.backward, oracle_sel=ref["slices"])
+    assert_close("o", got["o"], ref["o"], w.dtype)
+    assert_lse(got["lse"], ref["lse"])
+    if w.backward:
+        for key in ("dq", "dk", "dv"):
+            assert_close(key, got[key], ref[key], w.dtype)
