@@ -3,9 +3,10 @@
 // general-shape path (any B, any d multiple of 8 up to 256).
 //
 // Method: Pith review of arXiv 2512.16615. "Core claim": each query block
-// attends the B tokens of each of its K selected fine blocks plus one coarse
-// K/V token per level, reweighted by W^(l) = B^l (KV Reweighting, referee
-// minor comment 2: read as + ln B^l on the logit). "What carries the
+// attends the B tokens of each of its K selected fine blocks plus coarse K/V
+// tokens of the enrichment levels (one per level, or K_l per level under the
+// ALLK rule: the enrichment columns), reweighted by W^(l) = B^l (KV
+// Reweighting, referee minor comment 2: read as + ln B^l on the logit). "What carries the
 // argument" and the referee's Sec. 4.3 / Figure 4 comments: the backward uses
 // only sparse indices; dK/dV run key-major over the CSC from the index
 // transpose; gradients of the pooled (coarse) keys and values return to the
@@ -415,13 +416,14 @@ void allow_smem(K kernel, size_t smem) {
 }  // namespace
 
 // Gradient of every pooled token used by enrichment: the sum, in ascending
-// query-block order, of the coarse partials of the query blocks that used it.
-// One warp per pooled row. Level-1 tokens are fine blocks their users also
-// selected (TOP1 picks from the selection), so the fine CSC column lists the
-// candidates (under ANCESTOR the level-1 token e is used by block e alone);
-// level l >= 2 tokens scan the level's ancestors (one token per ancestor,
-// shared by its B^(l-1) query blocks) and add each hit ancestor's span sum,
-// which coarse_span_kernel left in the row of its first block. Candidates are tested 32
+// query-block order, of the coarse partials (one row per query block and
+// enrichment column) of the query blocks that used it. One warp per pooled
+// row. Level-1 tokens are fine blocks their users also selected (TOP1 and
+// ALLK pick from the selection), so the fine CSC column lists the candidates
+// (under ANCESTOR the level-1 token e is used by block e alone); level l >= 2
+// tokens scan the level's ancestors (each ancestor's tokens are shared by its
+// B^(l-1) query blocks) and add each hit ancestor's span sum, which
+// coarse_span_kernel left in the row of its first block. Candidates are tested 32
 // at a time (one per lane), the hits compacted in lane order, and their rows
 // summed in that order with several rows in flight; each lane owns kCols
 // consecutive columns.

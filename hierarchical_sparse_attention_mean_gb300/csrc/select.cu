@@ -1,4 +1,4 @@
-// select.cu -- hierarchical Top-K selection and the TOP1 enrichment index.
+// select.cu -- hierarchical Top-K selection and the enrichment index.
 //
 // Method: Pith review of arXiv 2512.16615, "Core claim" and "What carries the
 // argument": the coarsest level computes full similarities and keeps the K
@@ -6,8 +6,10 @@
 // kept above and carries the indices down (referee comment on Algorithm 1: the
 // parent-to-child map is read as contiguous, children of j are jB..jB+B-1).
 // Scores are raw dot products of pooled Q and K in fp32; ties go to the lower
-// index; stored rows are ascending. The enrichment token of level l for query
-// block i is the rank-1 choice of level l for i's ancestor floor(i / B^(l-1)).
+// index; stored rows are ascending. The enrichment tokens of level l for
+// query block i come from level l's row of i's ancestor floor(i / B^(l-1)):
+// its rank-1 choice (TOP1), the ancestor itself (ANCESTOR) or the whole
+// ascending row (ALLK), written into level l's columns of i's coarse row.
 //
 // One launch per level, coarsest first (each level needs the one above). A CTA
 // owns up to 16 sibling query rows that share one candidate list: candidate
