@@ -137,7 +137,8 @@ def work_model(w: synth.Workload, s) -> dict:
             # writes dq, the (lse, D) pairs and the pooled-level partials
             "bwd_dq": (6 * tok + bh * n * 12 + 2 * bh * s.n_blocks * s.enrich_cols * d * 4, 6 * d * pairs),
             "bwd_dkv": (6 * tok + bh * n * 8, 8 * d * fine_pairs),
-            "transpose": (4 * bh * s.n_blocks * s.topk_level[1] * 3, 0),
+            # reads the selection, writes row_idx and col_ptr (each once)
+            "transpose": (4 * bh * (2 * s.n_blocks * s.topk_level[1] + s.n_blocks + 1), 0),
             "select_level": (0, 2 * d * scored * bh),
         },
     }
