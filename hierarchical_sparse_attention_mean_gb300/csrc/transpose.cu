@@ -7,8 +7,8 @@
 // [11] of the paper): count the entries of each column, exclusive-scan the
 // counts into column pointers, scatter the row numbers.
 //
-// One kernel per call where a slice fits the shared memory of eight CTAs
-// (every workload of the paper's scale): a cluster of eight CTAs per slice.
+// One kernel per call where a slice fits the shared memory of eight CTAs and
+// all slices' clusters are resident at once: a cluster of eight CTAs per slice.
 //   1. CTA r takes rows [r R, (r+1) R) of the slice: it counts their entries
 //      per column in shared memory, scans the counts, and places each row
 //      number in its column's run (shared-memory atomics choose the slot);
@@ -506,34 +506,36 @@ transpose_cluster_kernel(const int* __restrict__ sel, int rows, int K, int ncols
 }
 
 // Whether the one-kernel transpose serves this shape: its shared memory fits
-// and a cluster of its CTAs can be resident (asked once per size class).
-bool cluster_fits(int rows, int K, int ncols, size_t* bytes) {
+// and every slice's cluster is resident at once. A second wave of clusters
+// doubles its time, and then the multi-kernel form, which spreads the entries
+// over every SM, is faster (measured at 512x512 tokens: 16 slices, 15
+// resident clusters). The resident-cluster count is asked once per size.
+bool cluster_serves(long long slices, int rows, int K, int ncols, size_t* bytes) {
     const ClLayout L = cl_layout(rows, K, ncols);
     *bytes = L.bytes;
     if (L.bytes > kClSmemMax || (long long)rows * K > INT_MAX) return false;
     static std::mutex mu;
-    static size_t ok_max = 0, bad_min = ~size_t(0);
+    static size_t last_bytes = 0;
+    static int last_clusters = 0;
     std::lock_guard<std::mutex> lk(mu);
-    if (L.bytes <= ok_max) return true;
-    if (L.bytes >= bad_min) return false;
-    if (cudaFuncSetAttribute(transpose_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClSmemMax) !=
-        cudaSuccess) {
-        cudaGetLastError();
-        bad_min = 0;
-        return false;
+    if (L.bytes != last_bytes) {
+        last_bytes = L.bytes;
+        last_clusters = 0;
+        if (cudaFuncSetAttribute(transpose_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kClSmemMax) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kCluster);
+        cfg.blockDim = dim3(kClThreads);
+        cfg.dynamicSmemBytes = L.bytes;
+        if (cudaOccupancyMaxActiveClusters(&last_clusters, transpose_cluster_kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            last_clusters = 0;
+        }
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kCluster);
-    cfg.blockDim = dim3(kClThreads);
-    cfg.dynamicSmemBytes = L.bytes;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, transpose_cluster_kernel, &cfg) != cudaSuccess || n < 1) {
-        cudaGetLastError();
-        bad_min = L.bytes;
-        return false;
-    }
-    ok_max = L.bytes;
-    return true;
+    return slices <= last_clusters;
 }
 
 }  // namespace
@@ -546,7 +548,7 @@ int launch_transpose(const Shape& s, const int32_t* sel, int rows, int K, int nc
     if (s.slices > 0x7fffffffLL) return LLSA_ERR_UNSUPPORTED;
     int* status = status_ptr();
     size_t cl_bytes = 0;
-    if (s.slices * (long long)kCluster <= 0x7fffffffLL && cluster_fits(rows, K, ncols, &cl_bytes)) {
+    if (cluster_serves(s.slices, rows, K, ncols, &cl_bytes)) {
         LLSA_LAUNCH("transpose", st,
                     transpose_cluster_kernel<<<(unsigned)(s.slices * kCluster), kClThreads, cl_bytes, st>>>(
                         sel, rows, K, ncols, col_ptr, row_idx, status));

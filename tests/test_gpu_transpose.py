@@ -2,8 +2,9 @@
 transpose, bit-exact, on selections shaped to reach every branch of the CUDA
 path: spatially local rows (the pixel workloads), uniform rows, unsorted rows,
 rows that all pick the same blocks (long column runs), fewer rows than the
-CTAs that share a slice, and a slice too large for the one-kernel form (the
-multi-kernel form then runs)."""
+CTAs that share a slice, and, for the multi-kernel form, a slice too large
+for the one-kernel form's shared memory and more slices than clusters that
+are resident at once."""
 import numpy as np
 import pytest
 import torch
@@ -61,6 +62,8 @@ CASES = {
     "n4096-B4-K3-uniform": (1, 2, 4096, 4, 3, "uniform"),
     # T = 32768 with K = 16: beyond the one-kernel form's shared memory
     "n524288-K16-multikernel": (1, 1, 524288, 16, 16, "uniform"),
+    # 64 slices: more clusters than are resident at once (multi-kernel form)
+    "n16384-64slices-local": (4, 16, 16384, 16, 8, "local"),
 }
 
 
