@@ -27,6 +27,25 @@ struct PoolArgs {
     LevelTable lv;
 };
 
+// Mean of B rows of a coarser level (float4 column vv of rows r*B..r*B+B-1
+// at row stride d), eight loads in flight, added in row order.
+__device__ __forceinline__ float4 mean_rows(const float* prev, long long r, int B, int d, int vv, float inv) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int c0 = 0; c0 < B; c0 += 8) {
+        float4 f[8];
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+            f[u] = c0 + u < B ? *reinterpret_cast<const float4*>(prev + (r * B + c0 + u) * d + vv * 4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; u++)
+            if (c0 + u < B) {
+                acc.x += f[u].x; acc.y += f[u].y; acc.z += f[u].z; acc.w += f[u].w;
+            }
+    }
+    return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
     const int tensor = blockIdx.y;
@@ -81,13 +100,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
         const int V = d / 4;
         for (int item = threadIdx.x; item < rows * V; item += kPoolThreads) {
             const int r = item / V, vv = item % V;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc = 0; cc < B; cc++) {
-                float4 f = *reinterpret_cast<const float4*>(prev + ((long long)r * B + cc) * d + vv * 4);
-                acc.x += f.x; acc.y += f.y; acc.z += f.z; acc.w += f.w;
-            }
-            *reinterpret_cast<float4*>(out + (long long)r * d + vv * 4) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            *reinterpret_cast<float4*>(out + (long long)r * d + vv * 4) = mean_rows(prev, r, B, d, vv, inv);
         }
         rows_prev = rows;
     }
@@ -108,13 +121,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_upper_kernel(PoolArgs a, in
         const int V = d / 4;
         for (int item = threadIdx.x; item < rows * V; item += kPoolThreads) {
             const int r = item / V, vv = item % V;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int cc = 0; cc < B; cc++) {
-                float4 f = *reinterpret_cast<const float4*>(prev + ((long long)r * B + cc) * d + vv * 4);
-                acc.x += f.x; acc.y += f.y; acc.z += f.z; acc.w += f.w;
-            }
-            *reinterpret_cast<float4*>(out + (long long)r * d + vv * 4) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            *reinterpret_cast<float4*>(out + (long long)r * d + vv * 4) = mean_rows(prev, r, B, d, vv, inv);
         }
     }
 }

@@ -509,17 +509,21 @@ transpose_cluster_kernel(const int* __restrict__ sel, int rows, int K, int ncols
 // and every slice's cluster is resident at once. A second wave of clusters
 // doubles its time, and then the multi-kernel form, which spreads the entries
 // over every SM, is faster (measured at 512x512 tokens: 16 slices, 15
-// resident clusters). The resident-cluster count is asked once per size.
+// resident clusters). The resident-cluster count is asked once per size and
+// device.
 bool cluster_serves(long long slices, int rows, int K, int ncols, size_t* bytes) {
     const ClLayout L = cl_layout(rows, K, ncols);
     *bytes = L.bytes;
     if (L.bytes > kClSmemMax || (long long)rows * K > INT_MAX) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
     static std::mutex mu;
     static size_t last_bytes = 0;
-    static int last_clusters = 0;
+    static int last_dev = -1, last_clusters = 0;
     std::lock_guard<std::mutex> lk(mu);
-    if (L.bytes != last_bytes) {
+    if (L.bytes != last_bytes || dev != last_dev) {
         last_bytes = L.bytes;
+        last_dev = dev;
         last_clusters = 0;
         if (cudaFuncSetAttribute(transpose_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kClSmemMax) != cudaSuccess) {
