@@ -20,10 +20,11 @@
 // block, group of eight) is one item; items follow the key blocks of the CTA
 // in order; the two warpgroups take alternate key blocks.
 //
-// Warp roles: three gather warps split every item's copies (warp 0 K_j, V_j
-// and the (lse, D) rows; warp 2 the Q stack; warp 3 the dO stack) into a ring
-// of stages; warp 1 issues the S stream and warp 12 the gradient stream, each
-// in order with blocking waits, through an election inside the MMA asm.
+// Warp roles: three gather warps split every item's copies (warp 0 K_j and
+// V_j; warp 2 the Q stack; warp 3 the dO stack) into a ring of stages, and
+// each softmax thread loads its query row's (lse, D) pair itself, one item
+// ahead; warp 1 issues the S stream and warp 12 the gradient stream, each in
+// order with blocking waits, through an election inside the MMA asm.
 #include <algorithm>
 
 #include "attn.h"
@@ -44,10 +45,9 @@ struct Cfg {
     static constexpr int REG = D / 64;
     static constexpr int QS_BYTES = 128 * D * 2;  // eight stacked 16-row query blocks
     static constexpr int KB_BYTES = 16 * D * 2;
-    // Q stack, dO stack, K_j, V_j, (lse, D) pairs of the 128 rows
+    // Q stack, dO stack, K_j, V_j
     static constexpr int OFF_DO = QS_BYTES, OFF_K = 2 * QS_BYTES, OFF_V = OFF_K + KB_BYTES;
-    static constexpr int OFF_LD = OFF_V + KB_BYTES;
-    static constexpr int STAGE_BYTES = OFF_LD + 1024;
+    static constexpr int STAGE_BYTES = OFF_V + KB_BYTES;
     // per warpgroup and buffer: dS^T and P^T of one item as K-major operands,
     // interleaved per 64 rows (dS^T chunk c at c * 4096, P^T chunk c at +2048)
     static constexpr int PG_BYTES = 8192;
@@ -66,7 +66,7 @@ struct Misc {
     // [group][buffer]: item buffers alternate with the group's items,
     // accumulators with its key blocks
     uint64_t full[6], empty[6];
-    uint64_t q_ready[2][2], s_full[2][2], s_free[2][2], p_full[2][2], p_free[2][2];
+    uint64_t s_full[2][2], s_free[2][2], p_full[2][2], p_free[2][2];
     uint64_t acc_full[2][2], acc_free[2][2], drain[2];
     uint32_t tmem_slot;
     int abort_flag;
@@ -137,7 +137,6 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         }
         for (int w = 0; w < 2; w++) {
             for (int b = 0; b < 2; b++) {
-                mbar_init(smem_u32(&ms->q_ready[w][b]), 1);
                 mbar_init(smem_u32(&ms->s_full[w][b]), 1);
                 mbar_init(smem_u32(&ms->s_free[w][b]), 128);
                 mbar_init(smem_u32(&ms->p_full[w][b]), 128);
@@ -213,7 +212,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             }
             unsigned char* sb = stages + st * C::STAGE_BYTES;
             const uint32_t fb = smem_u32(&ms->full[st]);
-            const uint32_t bytes = role == 0 ? 2 * C::KB_BYTES + nv * 128 : nv * C::KB_BYTES;
+            const uint32_t bytes = role == 0 ? 2 * C::KB_BYTES : nv * C::KB_BYTES;
             if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
             __syncwarp();
             const long long tok = slice * a.n + (long long)qb * 16;
@@ -225,7 +224,6 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                         tma_load_2d(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, yk, fb);
                     }
                 }
-                if (lane < nv) bulk_load(smem_u32(sb + C::OFF_LD + lane * 128), a.Dbuf + 2 * tok, 128, fb);
             } else if (lane < nv) {
                 const int off = role == 1 ? 0 : C::OFF_DO;
                 const CUtensorMap* map = role == 1 ? &mq : &mdo;
@@ -250,7 +248,6 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         const uint64_t dPB = desc_sw128(smem_u32(pbuf), 16, 1024);
         auto issue_S = [&](const ItemWalk& it) {
             const int st = it.n % C::STAGES;
-            if (lane == 0) mbar_arrive(smem_u32(&ms->q_ready[it.w][it.k & 1]));  // the group may read the stage
             tc_fence_after();
             const uint32_t s0 = (uint32_t)(st * C::STAGE_BYTES);
             const uint32_t tg = tbase + it.w * C::TM_GROUP + (it.k & 1) * 32;
@@ -383,6 +380,20 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 for (int c = 0; c < 16; c++) dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
             }
         };
+        // (lse, D) of this thread's query row for one of the group's items,
+        // loaded one item ahead of its use, so the two dependent loads (the
+        // CSC row, then the pair) hide behind the item before
+        auto load_ld = [&](int kb2, int gi2) -> float2 {
+            if (kb2 >= n_kb || tq >= 16 * min(8, kcnt[kb2] - 8 * gi2)) return make_float2(0.f, 0.f);
+            const long long g2 = blockIdx.x + (long long)kb2 * G;
+            const long long sl2 = g2 / a.T;
+            int qb2 = a.row_idx[sl2 * a.T * a.K1 + kbeg[kb2] + 8 * gi2 + (tq >> 4)];
+            if (qb2 < 0 || qb2 >= a.T) qb2 = 0;  // reported by the gather warps
+            return *reinterpret_cast<const float2*>(a.Dbuf + 2 * (sl2 * a.n + (long long)qb2 * 16 + (tq & 15)));
+        };
+        int kbn = w, gin = 0;  // the group's next item
+        while (kbn < n_kb && kcnt[kbn] == 0) kbn += 2;
+        float2 ld_next = load_ld(kbn, gin);
         for (int kb = w; kb < n_kb; kb += 2) {
             const long long g = blockIdx.x + (long long)kb * G;
             const long long slice = g / a.T;
@@ -405,14 +416,19 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 }
             }
             for (int gi = 0; gi < items; gi++, k++) {
-                const int n = kitem[kb] + gi;
-                const unsigned char* sb = stages + (n % C::STAGES) * C::STAGE_BYTES;
                 const bool row_ok = tq < 16 * min(8, cnt - 8 * gi);
                 // waits return at once after a timeout; the group keeps walking
                 const int b = k & 1;
                 const uint32_t ph = (uint32_t)(k >> 1) & 1;
-                mbar_wait(smem_u32(&ms->q_ready[w][b]), ph, abort_flag, a.status);
-                const float2 ld = *reinterpret_cast<const float2*>(sb + C::OFF_LD + tq * 8);  // (lse, D)
+                const float2 ld = ld_next;  // (lse, D)
+                if (8 * (gin + 1) < kcnt[kbn]) {
+                    gin++;
+                } else {
+                    gin = 0;
+                    do kbn += 2;
+                    while (kbn < n_kb && kcnt[kbn] == 0);
+                }
+                ld_next = load_ld(kbn, gin);
                 const float lse2 = ld.x * kLog2e, Dq = ld.y;
                 mbar_wait(smem_u32(&ms->s_full[w][b]), ph, abort_flag, a.status);
                 tc_fence_after();
