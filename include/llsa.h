@@ -159,7 +159,11 @@ int llsa_fwd(const llsa_params *p, const void *q, const void *k, const void *v, 
  *             prefix sum of the counts of columns < j (col_ptr[T] = T*K_1).
  *   row_idx : output int32 [batch*heads][T * K_1]; entries col_ptr[j] ..
  *             col_ptr[j+1]-1 list, ascending, every i with j in sel_idx[i].
- * Bit-exact and deterministic. */
+ *   ws      : llsa_workspace_bytes(p, LLSA_OP_TRANSPOSE) bytes, 16-byte
+ *             aligned (column counters; the one-kernel form leaves it unused).
+ * Bit-exact and deterministic. An entry outside [0, T) is skipped and
+ * reported through llsa_get_status (col_ptr[T] then counts the valid
+ * entries). Too small a workspace: LLSA_ERR_WORKSPACE, nothing enqueued. */
 int llsa_index_transpose(const llsa_params *p, const int32_t *sel_idx, int32_t *col_ptr, int32_t *row_idx,
                          void *ws, size_t ws_bytes, void *stream);
 
@@ -192,10 +196,12 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture.
- *   - Sharing: every call uses the same array. It is zeroed on the stream at
- *     the start of each call, so no earlier contents leak into a result, but
- *     calls whose kernels overlap on the GPU (different streams, no ordering)
- *     race on it and give wrong results. */
+ *   - Sharing: the multi-kernel form of the transpose (slices too large for
+ *     the one-kernel form, or more slices than resident thread-block
+ *     clusters) uses the array; every such call uses the same array. It is
+ *     zeroed on the stream at the start of each call, so no earlier contents
+ *     leak into a result, but such calls whose kernels overlap on the GPU
+ *     (different streams, no ordering) race on it and give wrong results. */
 #define LLSA_NOALLOC_TRANSPOSE_MAX_COUNTERS (1 << 20)
 int llsa_index_transpose_noalloc(const llsa_params *p, const int32_t *sel_idx, int32_t *col_ptr, int32_t *row_idx,
                                  void *stream);
