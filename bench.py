@@ -144,6 +144,15 @@ def work_model(w: synth.Workload, s) -> dict:
     }
 
 
+def spread(values):
+    """Median and 10th / 90th percentiles (nearest rank) of per-step times, ms."""
+    if not values:
+        return None
+    v = sorted(values)
+    at = lambda q: v[min(len(v) - 1, max(0, int(round(q * (len(v) - 1)))))]
+    return {"p10": round(at(0.1), 4), "median": round(at(0.5), 4), "p90": round(at(0.9), 4)}
+
+
 def kernel_key(name: str) -> str:
     for key in ("pool_chunk", "bwd_dq", "bwd_dkv", "select_level", "coarse_reduce"):
         if name.startswith(key):
@@ -269,11 +278,14 @@ def run_llsa(args, ws, rank, local):
     barrier()
     torch.cuda.synchronize()
     launches0 = llsa.llsa_launch_count()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # an event at every step boundary: the first and last bracket the timed
+    # region, the others give the spread of single steps
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    e0, e1 = marks[0], marks[-1]
     e0.record(stream)
-    for _ in range(args.steps):
+    for k in range(args.steps):
         step()
-    e1.record(stream)
+        marks[k + 1].record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
@@ -290,6 +302,17 @@ def run_llsa(args, ws, rank, local):
         tot, cnt = per.get(k, (0.0, 0))
         per[k] = (tot + ms, cnt + 1)
     stage_ms = {k: round(t / args.steps, 4) for k, (t, c) in per.items()}
+    step_each = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps)]
+    stage_each = {}  # stage -> per-step sums (every step launches the same kernels in order)
+    if args.steps > 0 and len(records) % args.steps == 0:
+        per_step = len(records) // args.steps
+        for k in range(args.steps):
+            sums = {}
+            for name, ms in records[k * per_step:(k + 1) * per_step]:
+                key = kernel_key(name)
+                sums[key] = sums.get(key, 0.0) + ms
+            for key, v in sums.items():
+                stage_each.setdefault(key, []).append(v)
     peaks, peak_src = load_peaks()
     work = work_model(w, s)
     dom = max(per, key=lambda k: per[k][0])
@@ -372,6 +395,7 @@ def run_llsa(args, ws, rank, local):
                    "flops_per_step": work["step_flops"], "flops_counted": "14*d per (query, key) pair: "
                    "fwd 4d, bwd 10d (S, dP, dV, dK, dQ); selection excluded"},
         "stage_ms": stage_ms,
+        "spread_ms": {"step": spread(step_each), **{k: spread(v) for k, v in stage_each.items()}},
         "stage_gbs": stage_gbs,
         "roofline": roof,
         "e2e": {"value": round(job_value(ws, work["step_flops"], e2e_ms), 3), "unit": "TFLOP/s",

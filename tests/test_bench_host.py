@@ -62,3 +62,10 @@ def test_sweep_entries_derive_or_are_refused(entry):
         return
     assert s.keys_per_query == s.topk_level[1] * B + s.enrich_cols
     assert s.levels == (L or s.levels)
+
+
+def test_spread_is_nearest_rank_percentiles():
+    assert bench.spread([]) is None
+    assert bench.spread([2.5]) == {"p10": 2.5, "median": 2.5, "p90": 2.5}
+    v = [float(x) for x in range(101)]  # 0 .. 100: the percentiles are the values themselves
+    assert bench.spread(list(reversed(v))) == {"p10": 10.0, "median": 50.0, "p90": 90.0}
