@@ -86,3 +86,35 @@ def test_transpose_matches_oracle(name):
         ref_cp, ref_ri = oracle.transpose(sel[sl], T)
         np.testing.assert_array_equal(cp[sl], ref_cp)
         np.testing.assert_array_equal(ri[sl], ref_ri)
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 16384, 16, 8), (1, 1, 524288, 16, 16)], ids=["cluster", "multikernel"])
+def test_transpose_skips_and_reports_out_of_range_entries(shape):
+    """An entry outside [0, T) is skipped by both forms and reported through
+    the status word; the valid entries form the CSC (brute force over the
+    input), col_ptr[T] counts them and nothing past that count is written."""
+    b, h, n, B, K = shape
+    p = llsa.Params(b, h, n, 64, block=B, topk=K)
+    s = llsa.get_sizes(p)
+    T = s.n_blocks
+    sel = _selection(s.slices, T, K, "uniform", seed=900 + T)
+    sel[0, 3, 2] = T + 5
+    sel[-1, 10, 0] = -1
+    col_ptr = torch.full((s.slices, T + 1), -7, dtype=torch.int32, device="cuda")
+    row_idx = torch.full((s.slices, T * K), -7, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(16, llsa.workspace_bytes(p, llsa.OP_TRANSPOSE)), dtype=torch.uint8, device="cuda")
+    llsa.llsa_index_transpose(p, torch.from_numpy(sel).cuda(), col_ptr, row_idx, ws)
+    torch.cuda.synchronize()
+    assert llsa.llsa_get_status() == -10
+    assert llsa.llsa_get_status() == 0
+    cp, ri = col_ptr.cpu().numpy(), row_idx.cpu().numpy()
+    for sl in range(s.slices):
+        rows = np.repeat(np.arange(T), K)
+        cols = sel[sl].reshape(-1)
+        keep = (cols >= 0) & (cols < T)
+        order = np.lexsort((rows[keep], cols[keep]))  # by column, then row
+        ref_ri = rows[keep][order]
+        ref_cp = np.concatenate([[0], np.cumsum(np.bincount(cols[keep], minlength=T))])
+        np.testing.assert_array_equal(cp[sl], ref_cp)
+        np.testing.assert_array_equal(ri[sl, :len(ref_ri)], ref_ri)
+        assert (ri[sl, len(ref_ri):] == -7).all()
