@@ -144,6 +144,46 @@ def work_model(w: synth.Workload, s) -> dict:
     }
 
 
+# Per-SM intake of scattered 2 KB copies into a ring of stages, measured by a
+# TMA microbenchmark on GB300 (one 128-row box per request; bytes per SM clock).
+GATHER_B_PER_CLK_SM = 23.9
+
+
+def gather_intake(w, s, b, stage_ms, clocks, dev):
+    """The tensor-core kernels' gathered bytes (every selected block and
+    stacked query block as it is copied into shared memory) per step, their
+    rate, and that rate against the per-SM copy-intake ceiling at the SM clock
+    seen in the timed region. A diagnostic beside the HBM roofline: these
+    kernels gather from L2, so HBM is not what binds them."""
+    import torch
+    if w.dtype != "bf16" or not clocks or not clocks.get("sm_mhz"):
+        return None
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ceiling = GATHER_B_PER_CLK_SM * sms * clocks["sm_mhz"] * 1e6  # bytes/s
+    blk = 16 * w.d * 2                                  # one 16-row block of a token tensor
+    pooled = 2 * s.enrich_cols * w.d * 4                # pooled K and V rows (fp32)
+    qblocks = w.bh * s.n_blocks
+    k1 = s.topk_level[1]
+    cnt = (b.col_ptr[:, 1:] - b.col_ptr[:, :-1]).to(torch.int64)
+    items = int(((cnt + 7) // 8).sum().item())
+    entries = int(cnt.sum().item())
+    gathered = {
+        "fwd": qblocks * (blk + 2 * k1 * blk + pooled),
+        "bwd_dq": qblocks * (3 * blk + 2 * k1 * blk + 64 + pooled),
+        "bwd_dkv": items * 2 * blk + entries * 2 * blk,
+    }
+    out = {}
+    for k, nbytes in gathered.items():
+        if k in stage_ms and stage_ms[k] > 0:
+            rate = nbytes / (stage_ms[k] * 1e-3)
+            out[k] = {"gathered_gb": round(nbytes / 1e9, 3), "tbs": round(rate / 1e12, 2),
+                      "frac": round(rate / ceiling, 3)}
+    return {"ceiling_tbs": round(ceiling / 1e12, 2),
+            "ceiling_source": f"{GATHER_B_PER_CLK_SM} B per SM clock (copy-intake microbenchmark) x {sms} SMs "
+                              f"x {clocks['sm_mhz']:.0f} MHz",
+            "kernels": out}
+
+
 def spread(values):
     """Median and 10th / 90th percentiles (nearest rank) of per-step times, ms."""
     if not values:
@@ -398,6 +438,7 @@ def run_llsa(args, ws, rank, local):
         "spread_ms": {"step": spread(step_each), **{k: spread(v) for k, v in stage_each.items()}},
         "stage_gbs": stage_gbs,
         "roofline": roof,
+        "gather_intake": gather_intake(w, s, b, stage_ms, clocks, dev) if tensor_path else None,
         "e2e": {"value": round(job_value(ws, work["step_flops"], e2e_ms), 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
