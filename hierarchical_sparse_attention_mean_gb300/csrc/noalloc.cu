@@ -26,6 +26,8 @@ int32_t* g_scratch_addr[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up once
 // per device (the array's name is only a host-side stand-in in host code).
+// The kept address does not survive cudaDeviceReset of that device; the
+// header tells such callers to reload the library.
 int scratch_on_current_device(int32_t** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LLSA_ERR_DEVICE;

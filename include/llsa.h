@@ -195,7 +195,11 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
  *   - Allocation: none; no cudaMalloc, cudaFree or allocating library call.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept for the life of the
+ *     process: after cudaDeviceReset of that device (or any other teardown of
+ *     its primary context) the kept address is stale, so such a caller
+ *     reloads the library before calling again. The device status word read
+ *     by llsa_get_status is looked up and kept the same way.
  *   - Sharing: the multi-kernel form of the transpose (slices too large for
  *     the one-kernel form, or more slices than resident thread-block
  *     clusters) uses the array; every such call uses the same array. It is

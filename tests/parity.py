@@ -6,7 +6,11 @@ Acceptance (the method's stated tolerances):
     except where the oracle's score of a differing index lies within 1e-3
     relative of the oracle's K-th score (a near-tie swap); the sparse index
     transpose bit-exact;
-  * o, dq, dk, dv: max-abs 2e-2 for bf16, max-abs <= 1e-4 * max|ref| for fp32;
+  * o, dq, dk, dv: max-abs 2e-2 for bf16; for fp32 max-abs <= 1e-4 * max|ref|
+    and, element by element, |got - ref| <= 1e-4 * |ref| + FP32_FLOOR * max|ref|
+    (the floor covers elements that cancel to near zero: fp32 accumulation
+    leaves them an absolute error of a few ulps of the terms summed, which are
+    bounded by the tensor's scale);
   * lse: abs 1e-3.
 No value computed by the CUDA path is ever fed to the oracle: stage tests feed
 the CUDA path the oracle's indices; the end-to-end test compares outputs only
@@ -25,6 +29,7 @@ from hierarchical_sparse_attention_mean_gb300 import synth
 TIE_REL = 1e-3
 BF16_ABS = 2e-2
 FP32_REL = 1e-4
+FP32_FLOOR = 1e-6   # absolute floor of the element-wise fp32 check, times max|ref| (~8 ulps)
 LSE_ABS = 1e-3
 
 
@@ -55,7 +60,9 @@ def out_tol_ok(got, ref, dtype):
     if dtype == "bf16":
         return err <= BF16_ABS, err
     scale = max(float(np.abs(ref).max()), 1e-30)
-    return err <= FP32_REL * scale, err / scale
+    # worst element against its own bound (<= 1 passes)
+    elem = float((np.abs(got - ref) / (FP32_REL * np.abs(ref) + FP32_FLOOR * scale)).max()) if got.size else 0.0
+    return err <= FP32_REL * scale and elem <= 1.0, max(err / scale, elem * FP32_REL)
 
 
 def assert_close(name, got, ref, dtype):

@@ -22,6 +22,11 @@ CASES = {
     # 768 query blocks: not a multiple of the SM count
     "ragged-h3": W("ragged", 1, 3, 4096, 64, amplitude=0.5, seed=77),
     "d128-K16": W("d128", 1, 2, 4096, 128, topk=16, amplitude=0.5, seed=78),
+    # the two tensor-core instances with fewer shared-memory stages (d = 64
+    # with K = 16; d = 128 with K = 8), on a ragged block count and on a
+    # spatially structured field
+    "d64-K16": W("d64k16", 1, 3, 4096, 64, topk=16, amplitude=0.5, seed=82),
+    "d128-K8-grf": W("d128k8", 1, 3, 4096, 128, topk=8, kind="grf", length_scale=4.0, grid=(64, 64), seed=83),
     "B4-L4-fp32": W("b4", 1, 2, 1024, 32, block=4, topk=3, dtype="fp32", seed=79),
     "B2-fig1": W("fig1", 1, 1, 8, 8, block=2, topk=1, dtype="fp32", seed=80),
     "B8-d16-bf16": W("b8", 2, 1, 512, 16, block=8, topk=5, amplitude=0.5, seed=81),
