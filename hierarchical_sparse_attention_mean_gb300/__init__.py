@@ -319,6 +319,7 @@ class Buffers:
         self.lse = torch.empty((p.batch, p.heads, p.n), dtype=torch.float32, device=dev)
         self.col_ptr = torch.empty((bh, s.n_blocks + 1), dtype=torch.int32, device=dev)
         self.row_idx = torch.empty((bh, s.n_blocks * s.topk_level[1]), dtype=torch.int32, device=dev)
+        self.ws_f = torch.empty(max(16, workspace_bytes(p, OP_FWD)), dtype=torch.uint8, device=dev)
         self.ws_t = torch.empty(max(16, workspace_bytes(p, OP_TRANSPOSE)), dtype=torch.uint8, device=dev)
         self.ws_b = torch.empty(max(16, workspace_bytes(p, OP_BWD)), dtype=torch.uint8, device=dev)
 
@@ -336,7 +337,7 @@ def forward(p: Params, q, k, v, bufs: Buffers | None = None, stream=None) -> Buf
     b = bufs or Buffers(p, q.device)
     llsa_pool(p, q, k, v, b.pyr, stream=stream)
     llsa_select(p, b.pyr, b.sel_idx, b.coarse_idx, b.level_idx, stream=stream)
-    llsa_fwd(p, q, k, v, b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse, stream=stream)
+    llsa_fwd(p, q, k, v, b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse, b.ws_f, stream=stream)
     return b
 
 

@@ -213,6 +213,7 @@ size_t llsa_workspace_bytes(const llsa_params* p, int op) {
     Shape s;
     if (derive(p, &s) != LLSA_OK) return 0;
     switch (op) {
+        case LLSA_OP_FWD: return fwd_workspace_bytes(s);
         case LLSA_OP_TRANSPOSE: return transpose_ws(s);
         case LLSA_OP_BWD: return bwd_workspace_bytes(s);
         default: return 0;
@@ -274,13 +275,15 @@ int llsa_select(const llsa_params* p, const float* pyr, int32_t* sel_idx, int32_
 int llsa_fwd(const llsa_params* p, const void* q, const void* k, const void* v, const float* pyr,
              const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, void* ws, size_t ws_bytes,
              void* stream) {
-    (void)ws; (void)ws_bytes;
     Shape s;
     LLSA_TRY(derive(p, &s));
     if (s.slices == 0) return LLSA_OK;
     LLSA_TRY(check_ptrs({q, k, v, pyr, sel_idx, coarse_idx, o, lse}));
+    const size_t need = fwd_workspace_bytes(s);
+    if (need > 0 && (!ws || ws_bytes < need)) return LLSA_ERR_WORKSPACE;
+    if (need > 0) LLSA_TRY(check_ptrs({ws}));
     LLSA_TRY(check_device());
-    return launch_fwd(s, q, k, v, pyr, sel_idx, coarse_idx, o, lse, static_cast<cudaStream_t>(stream));
+    return launch_fwd(s, q, k, v, pyr, sel_idx, coarse_idx, o, lse, ws, static_cast<cudaStream_t>(stream));
 }
 
 int llsa_index_transpose(const llsa_params* p, const int32_t* sel_idx, int32_t* col_ptr, int32_t* row_idx,

@@ -4,13 +4,21 @@
 
 namespace llsa {
 
+size_t fwd_workspace_bytes(const Shape& s) { return fwd_grp_supported(s) ? group_workspace_bytes(s) : 0; }
+
 int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, const float* pyr,
-               const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, cudaStream_t st) {
+               const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, void* ws, cudaStream_t st) {
     AttnArgs a = make_attn_args(s);
     a.q = q; a.k = k; a.v = v;
     a.kpyr = pyr + s.slices * a.pyr_stride;
     a.vpyr = pyr + 2 * s.slices * a.pyr_stride;
     a.sel = sel_idx; a.coarse = coarse_idx; a.out_o = o; a.lse = lse;
+    if (fwd_grp_supported(s)) {
+        int32_t *order, *gdesc, *ngroups;
+        carve_group_workspace(s, ws, &order, &gdesc, &ngroups);
+        LLSA_TRY(launch_group(s, sel_idx, order, gdesc, ngroups, st));
+        return launch_fwd_grp(s, a, order, gdesc, ngroups, st);
+    }
     if (fwd_tc_supported(s)) return launch_fwd_tc(s, a, st);
     return launch_fwd_simt(s, a, st);
 }

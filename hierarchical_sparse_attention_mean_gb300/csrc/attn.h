@@ -39,6 +39,17 @@ int launch_bwd_dq_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 
+// groups of query blocks sharing their selected key blocks (group.cu) and the
+// grouped tensor-core forward over them (bf16, B = 16, d = 64, K_1 in {8, 16})
+bool group_supported(const Shape& s);
+size_t group_workspace_bytes(const Shape& s);
+void carve_group_workspace(const Shape& s, void* ws, int32_t** order, int32_t** gdesc, int32_t** ngroups);
+int launch_group(const Shape& s, const int32_t* sel, int32_t* order, int32_t* gdesc, int32_t* ngroups,
+                 cudaStream_t st);
+bool fwd_grp_supported(const Shape& s);
+int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* order, const int32_t* gdesc,
+                   const int32_t* ngroups, cudaStream_t st);
+
 // tensor-core kernels (bf16, B = 16, d in {64, 128}, K_1 in {8, 16})
 bool fwd_tc_supported(const Shape& s);
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);

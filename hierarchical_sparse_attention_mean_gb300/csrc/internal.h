@@ -84,8 +84,9 @@ int device_ready();
 int launch_pool(const Shape& s, const void* q, const void* k, const void* v, float* pyr, cudaStream_t st);
 int launch_select(const Shape& s, const float* pyr, int32_t* sel_idx, int32_t* coarse_idx, int32_t* level_idx,
                   cudaStream_t st);
+size_t fwd_workspace_bytes(const Shape& s);
 int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, const float* pyr,
-               const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, cudaStream_t st);
+               const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, void* ws, cudaStream_t st);
 int launch_select_exhaustive(const Shape& s, const float* pyr, int32_t* out, cudaStream_t st);
 int launch_reorder(const Shape& s, int side, int root, int digits, const void* in, void* out, int inverse,
                    cudaStream_t st);

@@ -146,7 +146,14 @@ int llsa_select(const llsa_params *p, const float *pyr, int32_t *sel_idx, int32_
  *   sel_idx    : int32 [batch*heads][T][K_1], entries in [0, T).
  *   coarse_idx : int32 [batch*heads][T][C], level-l entries in [0, n_l).
  *   o          : output [batch, heads, N, d] (p->dtype).
- *   lse        : output fp32 [batch, heads, N] (natural log). */
+ *   lse        : output fp32 [batch, heads, N] (natural log).
+ *   ws         : llsa_workspace_bytes(p, LLSA_OP_FWD) bytes, 16-byte aligned
+ *                (0 bytes, ws may be NULL, where that is 0): the grouping of
+ *                query blocks that share selected key blocks, which the
+ *                tensor-core forward gathers once per group. Too small a
+ *                workspace: LLSA_ERR_WORKSPACE, nothing enqueued.
+ * A key block listed twice in a row of sel_idx counts once (the key set is
+ * the union of the listed blocks). */
 int llsa_fwd(const llsa_params *p, const void *q, const void *k, const void *v, const float *pyr,
              const int32_t *sel_idx, const int32_t *coarse_idx, void *o, float *lse,
              void *ws, size_t ws_bytes, void *stream);

@@ -154,7 +154,7 @@ def gpu_stage_outputs(w, x, p=None, backward=True, oracle_sel=None):
     if oracle_sel is not None:
         b.sel_idx.copy_(torch.from_numpy(np.stack([r["sel"]["levels"][1] for r in oracle_sel])))
         b.coarse_idx.copy_(torch.from_numpy(np.stack([r["sel"]["coarse"] for r in oracle_sel])))
-    llsa.llsa_fwd(p, d["q"], d["k"], d["v"], b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse)
+    llsa.llsa_fwd(p, d["q"], d["k"], d["v"], b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse, b.ws_f)
     out["o"] = f64(b.o).reshape(-1, w.n, w.d)
     out["lse"] = f64(b.lse).reshape(-1, w.n)
     llsa.llsa_index_transpose(p, b.sel_idx, b.col_ptr, b.row_idx, b.ws_t)

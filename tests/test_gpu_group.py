@@ -1,0 +1,89 @@
+"""The grouping of query blocks that the tensor-core forward gathers together
+(csrc/group.cu), read back from the forward's workspace and checked
+bit-exact against a numpy restatement of its rule: the anchor of query block
+i is the selected key block with the smallest bit-reversed index; query
+blocks sorted by (anchor, i); runs of equal anchors cut into groups of at most
+8. The groups must partition the query blocks, whatever the selection. The
+grouping changes no result, so the forward parity tests cover its use."""
+import numpy as np
+import pytest
+import torch
+
+import hierarchical_sparse_attention_mean_gb300 as llsa
+from hierarchical_sparse_attention_mean_gb300 import build, synth
+
+from parity import dev_inputs, params_of
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+
+
+def bitrev(j, bits):
+    j = np.asarray(j, np.int64)
+    r = np.zeros_like(j)
+    for b in range(bits):
+        r |= ((j >> b) & 1) << (bits - 1 - b)
+    return r
+
+
+def expected_groups(sel, T):
+    bits = int(np.ceil(np.log2(T))) if T > 1 else 0
+    h = bitrev(sel, bits)
+    anchor = sel[np.arange(T), np.argmin(h, axis=1)]
+    order = np.lexsort((np.arange(T), anchor))
+    groups = []
+    p = 0
+    while p < T:
+        q = p
+        while q < T and anchor[order[q]] == anchor[order[p]]:
+            q += 1
+        for s0 in range(p, q, 8):
+            groups.append((s0, min(8, q - s0)))
+        p = q
+    return order, groups
+
+
+def read_groups(b, slices, T):
+    ws = b.ws_f.view(torch.int32).cpu().numpy()
+    a = ((4 * slices * T + 255) // 256) * 256 // 4
+    order = ws[:slices * T].reshape(slices, T)
+    gdesc = ws[a:a + slices * T].reshape(slices, T)
+    ngroups = ws[2 * a:2 * a + slices]
+    return order, gdesc, ngroups
+
+
+@pytest.mark.parametrize("name", ["llsa-fwd-n4096-d64-b2h8-K8-bf16", "grf-64x64-K16", "n65536-grf-2heads"])
+def test_grouping_rule_and_partition(name):
+    if name == "grf-64x64-K16":
+        w = synth.Workload("g", 1, 3, 4096, 64, topk=16, kind="grf", length_scale=4.0, grid=(64, 64), seed=91)
+    elif name == "n65536-grf-2heads":
+        w = synth.Workload("g2", 1, 2, 65536, 64, kind="grf", length_scale=8.0, grid=(256, 256), seed=92)
+    else:
+        w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w, with_dout=False)
+    p = params_of(w)
+    d = dev_inputs(w, x)
+    b = llsa.forward(p, d["q"], d["k"], d["v"])
+    torch.cuda.synchronize()
+    assert llsa.llsa_get_status() == 0
+    s = llsa.get_sizes(p)
+    T = s.n_blocks
+    order, gdesc, ngroups = read_groups(b, s.slices, T)
+    sel = b.sel_idx.cpu().numpy()
+    sizes = []
+    for sl in range(s.slices):
+        ref_order, ref_groups = expected_groups(sel[sl], T)
+        np.testing.assert_array_equal(order[sl], ref_order)
+        assert ngroups[sl] == len(ref_groups)
+        got = [(int(g) & 0xFFFF, int(g) >> 16) for g in gdesc[sl, :ngroups[sl]]]
+        assert got == ref_groups
+        covered = np.concatenate([order[sl][a0:a0 + c] for a0, c in got])
+        assert sorted(covered.tolist()) == list(range(T))   # a partition
+        sizes += [c for _, c in got]
+    if w.kind == "grf":
+        # spatially structured selections group well (several blocks per group)
+        assert np.mean(sizes) > 3.0, np.mean(sizes)

@@ -215,7 +215,7 @@ def test_out_of_range_index_sets_status():
     torch.cuda.synchronize()
     assert llsa.llsa_get_status() == 0
     b.sel_idx[0, 3, 2] = 10_000
-    llsa.llsa_fwd(p, x["q"], x["k"], x["v"], b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse)
+    llsa.llsa_fwd(p, x["q"], x["k"], x["v"], b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse, b.ws_f)
     assert llsa.llsa_get_status() == -10
     assert llsa.llsa_get_status() == 0   # reading clears it
 
