@@ -167,8 +167,10 @@ def gather_intake(w, s, b, stage_ms, clocks, dev):
     cnt = (b.col_ptr[:, 1:] - b.col_ptr[:, :-1]).to(torch.int64)
     items = int(((cnt + 7) // 8).sum().item())
     entries = int(cnt.sum().item())
+    fwd_blocks = grouped_fwd_blocks(b, s)  # key blocks the grouped forward gathers (K and V each)
     gathered = {
-        "fwd": qblocks * (blk + 2 * k1 * blk + pooled),
+        "fwd": (qblocks * blk + 2 * fwd_blocks * blk + qblocks * pooled) if fwd_blocks is not None
+        else qblocks * (blk + 2 * k1 * blk + pooled),
         "bwd_dq": qblocks * (3 * blk + 2 * k1 * blk + 64 + pooled),
         "bwd_dkv": items * 2 * blk + entries * 2 * blk,
     }
@@ -182,6 +184,37 @@ def gather_intake(w, s, b, stage_ms, clocks, dev):
             "ceiling_source": f"{GATHER_B_PER_CLK_SM} B per SM clock (copy-intake microbenchmark) x {sms} SMs "
                               f"x {clocks['sm_mhz']:.0f} MHz",
             "kernels": out}
+
+
+def grouped_fwd_blocks(b, s, window: int = 1024):
+    """Key blocks the grouped tensor-core forward gathers in one step: for
+    every group of query blocks (read back from the forward's workspace), the
+    size of the union of their selections. None when the forward took no
+    workspace (no grouping)."""
+    import numpy as np
+    import torch
+    T, slices = s.n_blocks, s.slices
+    if b.ws_f.numel() < 8 * slices * T:
+        return None
+    windows = (T + window - 1) // window
+    ws = b.ws_f.view(torch.int32).cpu().numpy()
+    a = ((4 * slices * T + 255) // 256) * 256 // 4
+    order = ws[:slices * T].reshape(slices, T)
+    gdesc = ws[a:a + slices * T].reshape(slices, T)
+    ngroups = ws[2 * a:2 * a + slices * windows].reshape(slices, windows)
+    sel = b.sel_idx.cpu().numpy().astype(np.int64)
+    total = 0
+    for sl in range(slices):
+        gid = np.empty(T, np.int64)
+        g0 = 0
+        for wi in range(windows):
+            gd = gdesc[sl, wi * window:wi * window + ngroups[sl, wi]]
+            for k, v in enumerate(gd):
+                start, c = int(v) & 0xFFFF, int(v) >> 16
+                gid[order[sl, start:start + c]] = g0 + k
+            g0 += len(gd)
+        total += np.unique(gid[:, None] * T + sel[sl]).size
+    return int(total)
 
 
 def spread(values):

@@ -42,6 +42,8 @@ int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 // groups of query blocks sharing their selected key blocks (group.cu) and the
 // grouped tensor-core forward over them (bf16, B = 16, d = 64, K_1 in {8, 16})
 bool group_supported(const Shape& s);
+constexpr int kGroupWindow = 1024;  // query blocks per grouping window
+int group_windows(const Shape& s);    // grouping windows per slice
 size_t group_workspace_bytes(const Shape& s);
 void carve_group_workspace(const Shape& s, void* ws, int32_t** order, int32_t** gdesc, int32_t** ngroups);
 int launch_group(const Shape& s, const int32_t* sel, int32_t* order, int32_t* gdesc, int32_t* ngroups,

@@ -94,7 +94,8 @@ struct GBar {
 
 struct GArgs {
     AttnArgs a;
-    const int32_t *order, *gdesc, *ngroups;
+    const int32_t *order, *gdesc, *ngroups;  // grouping (group.cu), per window of query blocks
+    int windows, win;                          // windows per slice, query blocks per window
 };
 
 __device__ __forceinline__ bool wait_all(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status) {
@@ -217,7 +218,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     }
     if (warp == 0) {
         long long tot = 0;
-        for (long long s = lane; s < a.slices; s += 32) tot += ga.ngroups[s];
+        for (long long u = lane; u < a.slices * ga.windows; u += 32) tot += ga.ngroups[u];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
         if (lane == 0) bar->total_groups = tot;
@@ -237,7 +238,8 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         // Warp 0 serves warpgroup 0 (the CTA's groups 0, 2, ...), warp 2
         // warpgroup 1 (groups 1, 3, ...).
         const int w = warp >> 1;
-        long long cur_slice = 0, cur_base = 0;  // walk of the per-slice group counts
+        long long cur_slice = 0, cur_base = 0;  // walk of the per-window group counts
+        int cur_win = 0;
         long long qissued = 0;                  // groups whose Q slot copies were issued
         constexpr int R = C::NU / 32;
         // The next group's description is loaded one group ahead: its query
@@ -256,12 +258,15 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             for (int r = 0; r < R; r++) n_v[r] = 0x7FFFFFFF;
             if (jn >= mineW[w]) return;
             const long long gi = blockIdx.x + (2 * jn + w) * G;
-            while (cur_slice < a.slices && gi >= cur_base + ga.ngroups[cur_slice]) {
-                cur_base += ga.ngroups[cur_slice];
-                cur_slice++;
+            while (cur_slice < a.slices && gi >= cur_base + ga.ngroups[cur_slice * ga.windows + cur_win]) {
+                cur_base += ga.ngroups[cur_slice * ga.windows + cur_win];
+                if (++cur_win == ga.windows) {
+                    cur_win = 0;
+                    cur_slice++;
+                }
             }
             n_slice = cur_slice;
-            const int gd = ga.gdesc[n_slice * T + (gi - cur_base)];
+            const int gd = ga.gdesc[n_slice * T + cur_win * ga.win + (int)(gi - cur_base)];
             const int start = gd & 0xFFFF;
             n_count = gd >> 16;
             n_qb = lane < n_count ? ga.order[n_slice * T + start + lane] : -1;
@@ -779,6 +784,8 @@ int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* order, cons
     ga.order = order;
     ga.gdesc = gdesc;
     ga.ngroups = ngroups;
+    ga.windows = group_windows(s);
+    ga.win = kGroupWindow;
     return s.K1 == 8 ? launch_k<8>(s, ga, mq, mk, mv, st) : launch_k<16>(s, ga, mq, mk, mv, st);
 }
 

@@ -126,7 +126,8 @@ def test_workspace_sizes(lib):
     p = llsa.Params(1, 12, 65536, 64)
     assert llsa.workspace_bytes(p, llsa.OP_TRANSPOSE) == 12 * 4096 * 4
     assert llsa.workspace_bytes(p, llsa.OP_BWD) > 12 * 65536 * 4
-    # the grouping of query blocks: order and group list per slice, group counts
+    # the grouping of query blocks: order and group list per slice, group
+    # counts per window of 1024 query blocks
     assert llsa.workspace_bytes(p, llsa.OP_FWD) == 2 * 12 * 4096 * 4 + 256
     # shapes the grouped forward does not take need no forward workspace
     assert llsa.workspace_bytes(llsa.Params(1, 2, 4096, 128, topk=16), llsa.OP_FWD) == 0

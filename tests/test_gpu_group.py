@@ -1,10 +1,11 @@
 """The grouping of query blocks that the tensor-core forward gathers together
 (csrc/group.cu), read back from the forward's workspace and checked
 bit-exact against a numpy restatement of its rule: the anchor of query block
-i is the selected key block with the smallest bit-reversed index; query
-blocks sorted by (anchor, i); runs of equal anchors cut into groups of at most
-8. The groups must partition the query blocks, whatever the selection. The
-grouping changes no result, so the forward parity tests cover its use."""
+i is the selected key block with the smallest bit-reversed index; within each
+window of 1024 consecutive query blocks, blocks sorted by (anchor, i) and runs
+of equal anchors cut into groups of at most 8. The groups must partition the
+query blocks, whatever the selection. The grouping changes no result, so the
+forward parity tests cover its use."""
 import numpy as np
 import pytest
 import torch
@@ -30,29 +31,38 @@ def bitrev(j, bits):
     return r
 
 
+WIN = 1024
+
+
 def expected_groups(sel, T):
+    """Per window: (order of its query blocks, [(start in the slice's order, count)])."""
     bits = int(np.ceil(np.log2(T))) if T > 1 else 0
     h = bitrev(sel, bits)
     anchor = sel[np.arange(T), np.argmin(h, axis=1)]
-    order = np.lexsort((np.arange(T), anchor))
-    groups = []
-    p = 0
-    while p < T:
-        q = p
-        while q < T and anchor[order[q]] == anchor[order[p]]:
-            q += 1
-        for s0 in range(p, q, 8):
-            groups.append((s0, min(8, q - s0)))
-        p = q
-    return order, groups
+    out = []
+    for w0 in range(0, T, WIN):
+        idx = np.arange(w0, min(T, w0 + WIN))
+        order = idx[np.lexsort((idx, anchor[idx]))]
+        groups = []
+        p = 0
+        while p < len(order):
+            q = p
+            while q < len(order) and anchor[order[q]] == anchor[order[p]]:
+                q += 1
+            for s0 in range(p, q, 8):
+                groups.append((w0 + s0, min(8, q - s0)))
+            p = q
+        out.append((order, groups))
+    return out
 
 
 def read_groups(b, slices, T):
+    windows = (T + WIN - 1) // WIN
     ws = b.ws_f.view(torch.int32).cpu().numpy()
     a = ((4 * slices * T + 255) // 256) * 256 // 4
     order = ws[:slices * T].reshape(slices, T)
     gdesc = ws[a:a + slices * T].reshape(slices, T)
-    ngroups = ws[2 * a:2 * a + slices]
+    ngroups = ws[2 * a:2 * a + slices * windows].reshape(slices, windows)
     return order, gdesc, ngroups
 
 
@@ -76,14 +86,16 @@ def test_grouping_rule_and_partition(name):
     sel = b.sel_idx.cpu().numpy()
     sizes = []
     for sl in range(s.slices):
-        ref_order, ref_groups = expected_groups(sel[sl], T)
-        np.testing.assert_array_equal(order[sl], ref_order)
-        assert ngroups[sl] == len(ref_groups)
-        got = [(int(g) & 0xFFFF, int(g) >> 16) for g in gdesc[sl, :ngroups[sl]]]
-        assert got == ref_groups
-        covered = np.concatenate([order[sl][a0:a0 + c] for a0, c in got])
-        assert sorted(covered.tolist()) == list(range(T))   # a partition
-        sizes += [c for _, c in got]
+        covered = []
+        for wi, (ref_order, ref_groups) in enumerate(expected_groups(sel[sl], T)):
+            w0 = wi * WIN
+            np.testing.assert_array_equal(order[sl, w0:w0 + len(ref_order)], ref_order)
+            assert ngroups[sl, wi] == len(ref_groups)
+            got = [(int(g) & 0xFFFF, int(g) >> 16) for g in gdesc[sl, w0:w0 + ngroups[sl, wi]]]
+            assert got == ref_groups
+            covered += [order[sl][a0:a0 + c] for a0, c in got]
+            sizes += [c for _, c in got]
+        assert sorted(np.concatenate(covered).tolist()) == list(range(T))   # a partition
     if w.kind == "grf":
         # spatially structured selections group well (several blocks per group)
         assert np.mean(sizes) > 3.0, np.mean(sizes)
