@@ -85,6 +85,7 @@ def _load():
     lib.llsa_strerror.argtypes = [ctypes.c_int]
     lib.llsa_strerror.restype = ctypes.c_char_p
     lib.llsa_launch_count.restype = ctypes.c_ulonglong
+    lib.llsa_test_set_wait_limit.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.llsa_profile_enable.argtypes = [ctypes.c_int]
     lib.llsa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), ctypes.c_int]
     _lib = lib
@@ -278,6 +279,16 @@ def llsa_get_status(stream=None) -> int:
     st = ctypes.c_int(0)
     _check(_load().llsa_get_status(_stream(stream), ctypes.byref(st)), "llsa_get_status")
     return st.value
+
+
+LLSA_TEST_NO_COPIES = 1
+
+
+def test_set_wait_limit(polls: int = 0, flags: int = 0):
+    """Failure-detection test hook (llsa_test_set_wait_limit): polls before a
+    bounded device wait gives up (0: the kernels' own limit) and test
+    switches (LLSA_TEST_NO_COPIES: the copy warps issue nothing)."""
+    _check(_load().llsa_test_set_wait_limit(int(polls), int(flags)), "llsa_test_set_wait_limit")
 
 
 def llsa_launch_count() -> int:

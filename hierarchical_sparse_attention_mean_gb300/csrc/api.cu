@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "internal.h"
+#include "tc.cuh"
 
 namespace llsa {
 
@@ -24,6 +25,8 @@ int* g_status_addr[kMaxDevices];
 int g_sm_count[kMaxDevices];
 int g_cc_ok[kMaxDevices];  // 0 unknown, 1 ok, -1 wrong device
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_wait_limit{0};  // 0: the kernels' own limit
+std::atomic<int> g_test_flags{0};
 
 struct ProfRecord {
     const char* name;
@@ -179,11 +182,25 @@ static int check_ptrs(std::initializer_list<const void*> ptrs) {
 
 static size_t transpose_ws(const Shape& s) { return (size_t)s.slices * s.T * sizeof(int32_t); }
 
+int wait_limit() {
+    const int v = g_wait_limit.load();
+    return v > 0 ? v : tc::kSpinLimit;
+}
+
+int test_flags() { return g_test_flags.load(); }
+
 }  // namespace llsa
 
 using namespace llsa;
 
 extern "C" {
+
+int llsa_test_set_wait_limit(int polls, int flags) {
+    if (flags & ~LLSA_TEST_NO_COPIES) return LLSA_ERR_INVALID_ARG;
+    g_wait_limit.store(polls > 0 ? polls : 0);
+    g_test_flags.store(flags);
+    return LLSA_OK;
+}
 
 int llsa_get_sizes(const llsa_params* p, llsa_sizes* out) {
     Shape s;

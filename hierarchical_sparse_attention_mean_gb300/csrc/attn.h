@@ -21,6 +21,8 @@ struct AttnArgs {
     float scale, lnB;
     LevelTable lv;
     int* status;
+    int spin;        // polls before a bounded wait gives up (kSpinLimit unless a test lowered it)
+    int test_flags;  // LLSA_TEST_* switches of llsa_test_set_wait_limit (0 in normal use)
     int rule;  // enrichment rule
     // enrichment columns: C per coarse row, Lc used (levels 1..Le); column c
     // holds a token of level col_level[c]; level l owns columns

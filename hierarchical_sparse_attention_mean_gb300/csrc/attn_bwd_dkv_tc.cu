@@ -195,12 +195,13 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         int kb, nv, qb, kb1 = 0, nv1 = 0, qb1 = 0;
         int issued = -1;
         if (n_items > 0) locate(0, kb1, nv1, qb1);
-        for (int n = 0; n < n_items; n++) {
+        const int ni = (a.test_flags & LLSA_TEST_NO_COPIES) ? 0 : n_items;  // failure-detection test
+        for (int n = 0; n < ni; n++) {
             kb = kb1; nv = nv1; qb = qb1;
             if (n + 1 < n_items) locate(n + 1, kb1, nv1, qb1);
             const int st = n % C::STAGES, u = n / C::STAGES;
             bool ok = true;
-            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
+            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status, a.spin);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
             const long long g = blockIdx.x + (long long)kb * G;
@@ -290,7 +291,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         // and broadcasting the outcome
         auto wait1 = [&](uint64_t* bar, uint32_t parity) -> bool {
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(smem_u32(bar), parity, abort_flag, a.status) ? 1 : 0;
+            if (lane == 0) ok = mbar_wait(smem_u32(bar), parity, abort_flag, a.status, a.spin) ? 1 : 0;
             return __shfl_sync(0xffffffffu, ok, 0) != 0;
         };
         ItemWalk it;
@@ -342,7 +343,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             // dk = scale * acc + pooled fold, dv = acc + pooled fold
             float kk[16], vv[16];
             if (pacc) {
-                mbar_wait(smem_u32(&ms->acc_full[w][pkn & 1]), (pkn >> 1) & 1, abort_flag, a.status);
+                mbar_wait(smem_u32(&ms->acc_full[w][pkn & 1]), (pkn >> 1) & 1, abort_flag, a.status, a.spin);
                 tc_fence_after();
                 const uint32_t ta = tg + 64 + (pkn & 1) * 32;
                 if (D == 64) {
@@ -430,7 +431,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 }
                 ld_next = load_ld(kbn, gin);
                 const float lse2 = ld.x * kLog2e, Dq = ld.y;
-                mbar_wait(smem_u32(&ms->s_full[w][b]), ph, abort_flag, a.status);
+                mbar_wait(smem_u32(&ms->s_full[w][b]), ph, abort_flag, a.status, a.spin);
                 tc_fence_after();
                 float s[16], dp[16];
                 tmem_ld16(tg + b * 32, s);
@@ -438,7 +439,7 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 tc_fence_before();
                 mbar_arrive(smem_u32(&ms->s_free[w][b]));
                 // the operands of this group's item before last (same buffer) must be consumed
-                if (k >= 2) mbar_wait(smem_u32(&ms->p_free[w][b]), ph ^ 1u, abort_flag, a.status);
+                if (k >= 2) mbar_wait(smem_u32(&ms->p_free[w][b]), ph ^ 1u, abort_flag, a.status, a.spin);
                 unsigned char* pb = pb0 + b * C::PG_BYTES;
 #pragma unroll
                 for (int c = 0; c < 16; c++) {

@@ -137,13 +137,14 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const uint32_t my_bytes = role == 0 ? 3 * C::Q_BYTES + 64 + 2 * Le * D * 4 : C::KV_BYTES;
         int ix0 = load_idx(0), ix1 = load_idx(1);
         long long issued = -1;
-        for (long long bl = 0; bl < mine; bl++) {
+        const long long nb = (a.test_flags & LLSA_TEST_NO_COPIES) ? 0 : mine;  // failure-detection test
+        for (long long bl = 0; bl < nb; bl++) {
             int ix = ix0;
             ix0 = ix1;
             ix1 = load_idx(bl + 2);
             const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
             bool ok = true;
-            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
+            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status, a.spin);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
             const long long g = blockIdx.x + bl * G;
@@ -270,7 +271,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             } else {
                 int stop = 0;
                 if (lane == 0) {
-                    if (++idle >= kSpinLimit) {
+                    if (++idle >= a.spin) {
                         *abort_flag = 1;
                         set_status(a.status, LLSA_ERR_TIMEOUT);
                         stop = 1;
@@ -310,7 +311,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             const float* sLse = reinterpret_cast<const float*>(sb + C::OFF_L);
             // waits return at once after a timeout; the group keeps walking the
             // same barriers so that no thread waits on another
-            mbar_wait(smem_u32(&ms->q_ready[w]), j & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->q_ready[w]), j & 1, abort_flag, a.status, a.spin);
             // D_t = dO_t . o_t and the pooled-key dots q_t . k_l, dO_t . v_l:
             // eight threads per query, one 16-byte chunk per 64 columns each
             {
@@ -398,7 +399,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 lse2[c] = l4.x * kLog2e; lse2[c + 1] = l4.y * kLog2e; lse2[c + 2] = l4.z * kLog2e; lse2[c + 3] = l4.w * kLog2e;
                 dsm[c] = d4.x; dsm[c + 1] = d4.y; dsm[c + 2] = d4.z; dsm[c + 3] = d4.w;
             }
-            mbar_wait(smem_u32(&ms->s_full[w]), j & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->s_full[w]), j & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
 #pragma unroll
             for (int t = 0; t < NT; t++) {
@@ -421,7 +422,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             mbar_arrive(smem_u32(&ms->ds_full[w]));
             // epilogue: dq^T plus the pooled keys' term, times scale; the
             // pooled-level partial gradients of this block
-            mbar_wait(smem_u32(&ms->g_full[w]), j & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->g_full[w]), j & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
             float q[16], gk[16], gv[16];
             tmem_ld16(tS + 64, q);

@@ -98,8 +98,9 @@ struct GArgs {
     int windows, win;                          // windows per slice, query blocks per window
 };
 
-__device__ __forceinline__ bool wait_all(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status) {
-    const bool ok = mbar_wait(mbar, parity, abort_flag, status);
+__device__ __forceinline__ bool wait_all(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status,
+                                         int limit) {
+    const bool ok = mbar_wait(mbar, parity, abort_flag, status, limit);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -394,7 +395,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         int v_ns = 0, v_yk = 0;  // the tile whose V boxes are pending
         auto issue_v = [&]() -> bool {
             const int stv = w * C::NKW + tv % C::NKW, use = tv / C::NKW;
-            if (use >= 1 && !wait_all(smem_u32(&bar->v_empty[stv]), (uint32_t)((use - 1) & 1), abort_flag, a.status))
+            if (use >= 1 && !wait_all(smem_u32(&bar->v_empty[stv]), (uint32_t)((use - 1) & 1), abort_flag, a.status, a.spin))
                 return false;
             const uint32_t fb = smem_u32(&bar->v_full[stv]);
             if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)(v_ns * 16 * D * 2));
@@ -404,9 +405,12 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             v_ns = 0;
             return true;
         };
+        // a failure-detection test can switch the copies off (nothing armed,
+        // every consumer's first wait runs out)
+        const long long jN = (a.test_flags & LLSA_TEST_NO_COPIES) ? 0 : mineW[w];
         bool ok = true;
-        if (mineW[w] > 0) setup(0);
-        for (long long j = 0; j < mineW[w] && ok; j++) {
+        if (jN > 0) setup(0);
+        for (long long j = 0; j < jN && ok; j++) {
             const int qsl = w * C::NQW + (int)(j % C::NQW);
             const Meta* meta = reinterpret_cast<const Meta*>(qslots + qsl * C::QSLOT + C::META_OFF);
             const int nslots = meta->nslots;
@@ -418,7 +422,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             for (int t = 0; t < nt && ok; t++) {
                 const int stk = w * C::NKW + tk % C::NKW, use = tk / C::NKW;
                 if (use >= 1 &&
-                    !wait_all(smem_u32(&bar->k_empty[stk]), (uint32_t)((use - 1) & 1), abort_flag, a.status)) {
+                    !wait_all(smem_u32(&bar->k_empty[stk]), (uint32_t)((use - 1) & 1), abort_flag, a.status, a.spin)) {
                     ok = false;
                     break;
                 }
@@ -434,10 +438,10 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 v_yk = yk;
             }
             // the next group, once its Q slot is free
-            if (ok && j + 1 < mineW[w]) {
+            if (ok && j + 1 < jN) {
                 const long long jn = j + 1, qu = jn / C::NQW;
                 if (qu >= 1 && !wait_all(smem_u32(&bar->q_empty[w * C::NQW + (int)(jn % C::NQW)]),
-                                         (uint32_t)((qu - 1) & 1), abort_flag, a.status))
+                                         (uint32_t)((qu - 1) & 1), abort_flag, a.status, a.spin))
                     ok = false;
                 else
                     setup(jn);
@@ -489,17 +493,17 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         auto issue_S = [&]() -> bool {
             const int qsl = w * C::NQW + (int)(gS % C::NQW);
             if (tS == 0) {
-                if (!wait_all(smem_u32(&bar->q_full[qsl]), (uint32_t)((gS / C::NQW) & 1), abort_flag, a.status))
+                if (!wait_all(smem_u32(&bar->q_full[qsl]), (uint32_t)((gS / C::NQW) & 1), abort_flag, a.status, a.spin))
                     return false;
                 nsl[gS & 3] = reinterpret_cast<const Meta*>(qslots + qsl * C::QSLOT + C::META_OFF)->nslots;
             }
             const int nslots = nsl[gS & 3];
             const int st = w * C::NKW + tauS % C::NKW;
             const int b = tauS & 1;
-            if (!wait_all(smem_u32(&bar->k_full[st]), (uint32_t)((tauS / C::NKW) & 1), abort_flag, a.status))
+            if (!wait_all(smem_u32(&bar->k_full[st]), (uint32_t)((tauS / C::NKW) & 1), abort_flag, a.status, a.spin))
                 return false;
             if (tauS >= 2 &&
-                !wait_all(smem_u32(&bar->s_free[w][b]), (uint32_t)(((tauS >> 1) - 1) & 1), abort_flag, a.status))
+                !wait_all(smem_u32(&bar->s_free[w][b]), (uint32_t)(((tauS >> 1) - 1) & 1), abort_flag, a.status, a.spin))
                 return false;
             tc_fence_after();
             const int ns = min(C::TS, nslots - tS * C::TS);
@@ -522,16 +526,16 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         };
         auto issue_PV = [&]() -> bool {
             const int b = tauP & 1;
-            if (!wait_all(smem_u32(&bar->p_full[w][b]), (uint32_t)((tauP >> 1) & 1), abort_flag, a.status))
+            if (!wait_all(smem_u32(&bar->p_full[w][b]), (uint32_t)((tauP >> 1) & 1), abort_flag, a.status, a.spin))
                 return false;
             if (tP == 0 && gP >= 1 &&
-                !wait_all(smem_u32(&bar->o_free[w]), (uint32_t)((gP - 1) & 1), abort_flag, a.status))
+                !wait_all(smem_u32(&bar->o_free[w]), (uint32_t)((gP - 1) & 1), abort_flag, a.status, a.spin))
                 return false;
             tc_fence_after();
             const int nslots = nsl[gP & 3];
             const int ns = min(C::TS, nslots - tP * C::TS);
             const int st = w * C::NKW + tauP % C::NKW;
-            if (!wait_all(smem_u32(&bar->v_full[st]), (uint32_t)((tauP / C::NKW) & 1), abort_flag, a.status))
+            if (!wait_all(smem_u32(&bar->v_full[st]), (uint32_t)((tauP / C::NKW) & 1), abort_flag, a.status, a.spin))
                 return false;
             tc_fence_after();
             const uint32_t v0 = (uint32_t)(st * C::KTILE);
@@ -577,7 +581,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             const int qsl = w * C::NQW + (int)(j % C::NQW);
             const unsigned char* slot = qslots + qsl * C::QSLOT;
             const Meta* meta = reinterpret_cast<const Meta*>(slot + C::META_OFF);
-            if (!wait_all(smem_u32(&bar->q_full[qsl]), (uint32_t)((j / C::NQW) & 1), abort_flag, a.status)) break;
+            if (!wait_all(smem_u32(&bar->q_full[qsl]), (uint32_t)((j / C::NQW) & 1), abort_flag, a.status, a.spin)) break;
             // the group's description, kept in registers
             const int count = meta->count, nslots = meta->nslots;
             const long long slice = meta->slice;
@@ -632,12 +636,12 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                 const int b = tau & 1;
                 const uint32_t use = (uint32_t)(tau >> 1);
                 const uint32_t tS = tS0 + b * 64, tP = tP0 + b * 32;
-                if (!wait_all(smem_u32(&bar->s_full[w][b]), use & 1, abort_flag, a.status)) {
+                if (!wait_all(smem_u32(&bar->s_full[w][b]), use & 1, abort_flag, a.status, a.spin)) {
                     ok = false;
                     break;
                 }
                 // P buffer b was last read by the P V product two tiles back
-                if (use >= 1 && !wait_all(smem_u32(&bar->pv_done[w][b]), (use - 1) & 1, abort_flag, a.status)) {
+                if (use >= 1 && !wait_all(smem_u32(&bar->pv_done[w][b]), (use - 1) & 1, abort_flag, a.status, a.spin)) {
                     ok = false;
                     break;
                 }
@@ -676,7 +680,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     if (t > 0) {
                         const int bp = (tau - 1) & 1;
                         if (!wait_all(smem_u32(&bar->pv_done[w][bp]), (uint32_t)(((tau - 1) >> 1) & 1), abort_flag,
-                                      a.status)) {
+                                      a.status, a.spin)) {
                             ok = false;
                             break;
                         }
@@ -693,7 +697,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
             // epilogue: O / row sum + pooled values
             {
                 const int bl = (tau - 1) & 1;
-                if (!wait_all(smem_u32(&bar->pv_done[w][bl]), (uint32_t)(((tau - 1) >> 1) & 1), abort_flag, a.status))
+                if (!wait_all(smem_u32(&bar->pv_done[w][bl]), (uint32_t)(((tau - 1) >> 1) & 1), abort_flag, a.status, a.spin))
                     break;
             }
             tc_fence_after();

@@ -148,7 +148,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         int issued = -1;
         for (int bl = pw;; bl += C::NPROD) {
             const long long g = blockIdx.x + (long long)bl * G;
-            if (g >= total) break;
+            if (g >= total || (a.test_flags & LLSA_TEST_NO_COPIES)) break;
             int jb = jb0, e = ce0;
             jb0 = jb1;
             ce0 = ce1;
@@ -156,7 +156,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             int st, u;
             stage_of<C>(bl, st, u);
             bool ok = true;
-            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
+            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status, a.spin);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
             const long long slice = g / a.T;
@@ -215,10 +215,10 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 const int w = bl & 1, j = bl >> 1;
                 int st, u;
                 stage_of<C>(bl, st, u);
-                if (!mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status, a.spin)) return false;
                 mbar_arrive(smem_u32(&ms->q_ready[w]));  // the group may read Q and pooled rows
                 // S columns of this group: free once the group has read its previous S
-                if (j >= 1 && !mbar_wait(smem_u32(&ms->s_free[w]), (j - 1) & 1, abort_flag, a.status)) return false;
+                if (j >= 1 && !mbar_wait(smem_u32(&ms->s_free[w]), (j - 1) & 1, abort_flag, a.status, a.spin)) return false;
                 tc_fence_after();
                 const uint32_t q0 = (uint32_t)(st * C::STAGE_BYTES), k0 = q0 + C::Q_BYTES;
 #pragma unroll
@@ -235,8 +235,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 const int w = bl & 1, j = bl >> 1;
                 int st, u;
                 stage_of<C>(bl, st, u);
-                if (!mbar_wait(smem_u32(&ms->p_full[w]), j & 1, abort_flag, a.status)) return false;
-                if (j >= 1 && !mbar_wait(smem_u32(&ms->o_free[w]), (j - 1) & 1, abort_flag, a.status)) return false;
+                if (!mbar_wait(smem_u32(&ms->p_full[w]), j & 1, abort_flag, a.status, a.spin)) return false;
+                if (j >= 1 && !mbar_wait(smem_u32(&ms->o_free[w]), (j - 1) & 1, abort_flag, a.status, a.spin)) return false;
                 tc_fence_after();
                 const uint32_t v0 = (uint32_t)(st * C::STAGE_BYTES + C::Q_BYTES + C::KV_BYTES);
                 const uint32_t p0 = (uint32_t)(w * C::P_BYTES);
@@ -300,7 +300,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             // q_ready (set by the MMA thread once it has seen the stage full) is
             // per group and in order; waiting on the stage barrier itself could
             // alias an older phase when stages are few.
-            mbar_wait(smem_u32(&ms->q_ready[w]), j & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->q_ready[w]), j & 1, abort_flag, a.status, a.spin);
             {
                 float acc0 = 0.f, acc1 = 0.f;
                 if (pact) {
@@ -328,7 +328,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
             for (int l = 0; l < 4; l++) vc[l] = (l < Le && valid) ? sCk[(4 + l) * D + dd] : 0.f;
 
-            mbar_wait(smem_u32(&ms->s_full[w]), j & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->s_full[w]), j & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
             float s[NT][16];
 #pragma unroll
@@ -408,7 +408,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tc_fence_before();
             mbar_arrive(smem_u32(&ms->p_full[w]));
             // epilogue: O^T from TMEM plus the pooled values, written as bf16 rows
-            mbar_wait(smem_u32(&ms->o_full[w]), j & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->o_full[w]), j & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
             float o[16];
             tmem_ld16(tO, o);
@@ -560,13 +560,14 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         const uint32_t my_bytes = role == 0 ? C::Q_BYTES + C::KV_BYTES : role == 1 ? C::KV_BYTES : 2 * Le * D * 4;
         int ix0 = load_idx(0), ix1 = load_idx(1);
         long long issued = -1;
-        for (long long bl = 0; bl < mine; bl++) {
+        const long long nb = (a.test_flags & LLSA_TEST_NO_COPIES) ? 0 : mine;  // failure-detection test
+        for (long long bl = 0; bl < nb; bl++) {
             int ix = ix0;
             ix0 = ix1;
             ix1 = load_idx(bl + 2);
             const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
             bool ok = true;
-            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status);
+            if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status, a.spin);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
             const long long g = blockIdx.x + bl * G;
@@ -687,7 +688,7 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             } else {
                 int stop = 0;
                 if (lane == 0) {
-                    if (++idle >= kSpinLimit) {
+                    if (++idle >= a.spin) {
                         *abort_flag = 1;
                         set_status(a.status, LLSA_ERR_TIMEOUT);
                         stop = 1;
@@ -719,7 +720,7 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
         auto coarse = [&](long long j, int cb) {
             const long long bl = w + 2 * j;
             const int st = (int)(bl % C::STAGES), u = (int)(bl / C::STAGES);
-            mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->full[st]), u & 1, abort_flag, a.status, a.spin);
             const unsigned char* sQ = stages + st * C::STAGE_BYTES;
             const float* sCk = reinterpret_cast<const float*>(sQ + C::Q_BYTES + 2 * C::KV_BYTES);
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -769,7 +770,7 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             const long long g = blockIdx.x + bl * G;
             const long long slice = g / a.T;
             const int i = (int)(g - slice * a.T);
-            mbar_wait(smem_u32(&ms->o_full[w][b]), use & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->o_full[w][b]), use & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
             float o[16];
             tmem_ld16(tbase + w * C::TM_GROUP + 2 * C::TM_S + b * 16 + lanes, o);
@@ -812,7 +813,7 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 const float4 v = *reinterpret_cast<const float4*>(&ms->cmax[w][cb][c]);
                 m2[c] = v.x; m2[c + 1] = v.y; m2[c + 2] = v.z; m2[c + 3] = v.w;
             }
-            mbar_wait(smem_u32(&ms->s_full[w][b]), use & 1, abort_flag, a.status);
+            mbar_wait(smem_u32(&ms->s_full[w][b]), use & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
             float s[NT][16];
 #pragma unroll

@@ -605,6 +605,8 @@ AttnArgs make_attn_args(const Shape& s) {
     a.lnB = logf((float)s.B);
     a.lv = level_table(s);
     a.status = status_ptr();
+    a.spin = wait_limit();
+    a.test_flags = test_flags();
     a.rule = s.rule;
     a.C = s.C;
     a.Lc = s.Lc;

@@ -75,6 +75,11 @@ int* status_ptr();
 // Number of SMs of the current device.
 int sm_count();
 
+// Polls before a bounded device wait gives up, and the test switches, as set
+// by llsa_test_set_wait_limit (defaults: the kernels' own limit, no switch).
+int wait_limit();
+int test_flags();
+
 // LLSA_OK when the current device is a GB300 (compute capability 10.3); also
 // sets up the per-device status word on first use.
 int device_ready();

@@ -104,11 +104,14 @@ __device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase of the given parity to complete. Gives up after a
-// bounded number of polls, or as soon as another thread of the CTA gave up
-// (abort flag), recording LLSA_ERR_TIMEOUT; returns false then.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status) {
-    for (int it = 0; it < kSpinLimit; it++) {
+// Waits for the phase of the given parity to complete. Gives up after
+// `limit` polls (the library's wait limit, kSpinLimit unless a test lowered
+// it), or as soon as another thread of the CTA gave up (abort flag),
+// recording LLSA_ERR_TIMEOUT; returns false then.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          int limit) {
+    if (*abort_flag) return false;
+    for (int it = 0; it < limit; it++) {
         if (mbar_try(mbar, parity)) return true;
         if ((it & 63) == 63 && *abort_flag) return false;
     }

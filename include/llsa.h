@@ -188,6 +188,19 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
              const int32_t *coarse_idx, const int32_t *col_ptr, const int32_t *row_idx,
              void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, void *stream);
 
+/* Test hook for failure detection; no counterpart in the paper. Sets how many
+ * polls a bounded device wait of the tensor-core kernels makes before it gives
+ * up and records LLSA_ERR_TIMEOUT in the status word (polls <= 0 restores the
+ * kernels' own limit, about a second of polling), and test switches:
+ *   LLSA_TEST_NO_COPIES  the kernels' copy warps issue no copies, so every
+ *                        consumer's first wait runs out with no copy or MMA in
+ *                        flight; the kernel then drains, frees its tensor
+ *                        memory and exits, leaving its outputs undefined.
+ * Process-wide; applies to calls made after it; (0, 0) is the default state.
+ * Host-side only, no device work. Unknown flag bits: LLSA_ERR_INVALID_ARG. */
+#define LLSA_TEST_NO_COPIES 1
+int llsa_test_set_wait_limit(int polls, int flags);
+
 /* Sparse index transpose for callers that cannot allocate device memory.
  * No counterpart in the paper: this is a deployment variant of
  * llsa_index_transpose for callers that may not call cudaMalloc or hand over a
