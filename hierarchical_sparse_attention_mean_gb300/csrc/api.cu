@@ -9,6 +9,8 @@
 #include <mutex>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 #include "tc.cuh"
 
@@ -182,6 +184,13 @@ static int check_ptrs(std::initializer_list<const void*> ptrs) {
 
 static size_t transpose_ws(const Shape& s) { return (size_t)s.slices * s.T * sizeof(int32_t); }
 
+// An NVTX range around a C-ABI call (the call's name), so a profiler timeline
+// shows each library call with the kernels it enqueued.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+};
+
 int wait_limit() {
     const int v = g_wait_limit.load();
     return v > 0 ? v : tc::kSpinLimit;
@@ -239,6 +248,7 @@ size_t llsa_workspace_bytes(const llsa_params* p, int op) {
 
 int llsa_pool(const llsa_params* p, const void* q, const void* k, const void* v, float* pyr, void* ws,
               size_t ws_bytes, void* stream) {
+    CallRange range("llsa_pool");
     (void)ws; (void)ws_bytes;
     Shape s;
     LLSA_TRY(derive(p, &s));
@@ -249,6 +259,7 @@ int llsa_pool(const llsa_params* p, const void* q, const void* k, const void* v,
 }
 
 int llsa_select_exhaustive(const llsa_params* p, const float* pyr, int32_t* sel_idx, void* stream) {
+    CallRange range("llsa_select_exhaustive");
     Shape s;
     LLSA_TRY(derive(p, &s));
     if (s.slices == 0) return LLSA_OK;
@@ -258,6 +269,7 @@ int llsa_select_exhaustive(const llsa_params* p, const float* pyr, int32_t* sel_
 }
 
 int llsa_reorder(const llsa_params* p, int height, int width, const void* in, void* out, int inverse, void* stream) {
+    CallRange range("llsa_reorder");
     Shape s;
     LLSA_TRY(derive(p, &s));
     if (inverse != 0 && inverse != 1) return LLSA_ERR_INVALID_ARG;
@@ -279,6 +291,7 @@ int llsa_reorder(const llsa_params* p, int height, int width, const void* in, vo
 
 int llsa_select(const llsa_params* p, const float* pyr, int32_t* sel_idx, int32_t* coarse_idx,
                 int32_t* level_idx, void* ws, size_t ws_bytes, void* stream) {
+    CallRange range("llsa_select");
     (void)ws; (void)ws_bytes;
     Shape s;
     LLSA_TRY(derive(p, &s));
@@ -292,6 +305,7 @@ int llsa_select(const llsa_params* p, const float* pyr, int32_t* sel_idx, int32_
 int llsa_fwd(const llsa_params* p, const void* q, const void* k, const void* v, const float* pyr,
              const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, void* ws, size_t ws_bytes,
              void* stream) {
+    CallRange range("llsa_fwd");
     Shape s;
     LLSA_TRY(derive(p, &s));
     if (s.slices == 0) return LLSA_OK;
@@ -305,6 +319,7 @@ int llsa_fwd(const llsa_params* p, const void* q, const void* k, const void* v, 
 
 int llsa_index_transpose(const llsa_params* p, const int32_t* sel_idx, int32_t* col_ptr, int32_t* row_idx,
                          void* ws, size_t ws_bytes, void* stream) {
+    CallRange range("llsa_index_transpose");
     Shape s;
     LLSA_TRY(derive(p, &s));
     if (s.slices == 0) return LLSA_OK;
@@ -320,6 +335,7 @@ int llsa_bwd(const llsa_params* p, const void* q, const void* k, const void* v, 
              const void* dout, const float* pyr, const int32_t* sel_idx, const int32_t* coarse_idx,
              const int32_t* col_ptr, const int32_t* row_idx, void* dq, void* dk, void* dv, void* ws,
              size_t ws_bytes, void* stream) {
+    CallRange range("llsa_bwd");
     Shape s;
     LLSA_TRY(derive(p, &s));
     if (s.slices == 0) return LLSA_OK;

@@ -15,9 +15,18 @@ int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, cons
     a.sel = sel_idx; a.coarse = coarse_idx; a.out_o = o; a.lse = lse;
     if (fwd_grp_supported(s)) {
         int32_t *order, *gdesc, *ngroups;
-        carve_group_workspace(s, ws, &order, &gdesc, &ngroups);
-        LLSA_TRY(launch_group(s, sel_idx, order, gdesc, ngroups, st));
-        return launch_fwd_grp(s, a, order, gdesc, ngroups, st);
+        GroupRec* recs;
+        carve_group_workspace(s, ws, &order, &gdesc, &ngroups, &recs);
+        GroupArgs g;
+        g.coarse = coarse_idx;
+        g.C = s.C;
+        g.Le = s.Le;
+        for (int l = 0; l < 4; l++) {
+            g.col[l] = l < s.Le ? s.col_off[l + 1] : 0;
+            g.n_level[l] = l < s.Le ? s.n_level[l + 1] : 1;
+        }
+        LLSA_TRY(launch_group(s, sel_idx, g, order, gdesc, ngroups, recs, st));
+        return launch_fwd_grp(s, a, ngroups, recs, st);
     }
     if (fwd_tc_supported(s)) return launch_fwd_tc(s, a, st);
     return launch_fwd_simt(s, a, st);

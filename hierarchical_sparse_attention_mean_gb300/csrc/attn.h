@@ -46,13 +46,39 @@ int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 bool group_supported(const Shape& s);
 constexpr int kGroupWindow = 1024;  // query blocks per grouping window
 int group_windows(const Shape& s);    // grouping windows per slice
+
+// Description of one group of query blocks (group.cu writes one per group at
+// the group's gdesc position; the grouped kernels copy it as it is): the
+// union U of the group's selected key blocks (ascending), which union blocks
+// each of its query blocks selected, the query blocks and their enrichment
+// tokens. 512 bytes, 16-byte aligned (copied as 16-byte pieces); indices fit
+// 16 bits (T <= 2^14).
+struct alignas(16) GroupRec {
+    uint32_t mask[8][4];        // bit u % 32 of word u / 32: union block u selected by query block q
+    unsigned short uni[128];    // union blocks, ascending (K_1 <= 16: at most 128)
+    unsigned short qb[8];       // the group's query blocks
+    unsigned short ce[8][4];    // enrichment token of query block q at level l + 1 (l < L_e <= 3)
+    int count, nslots;          // query blocks, union blocks
+    int slice;
+    int pad[9];
+};
+static_assert(sizeof(GroupRec) == 512 && alignof(GroupRec) == 16, "group record");
+
+// What the grouping needs beyond the selection: the enrichment columns.
+struct GroupArgs {
+    const int32_t* coarse;  // [slices][T][C]
+    int C, Le;
+    int col[4];             // column of level l + 1
+    int n_level[4];         // tokens of level l + 1
+};
 size_t group_workspace_bytes(const Shape& s);
-void carve_group_workspace(const Shape& s, void* ws, int32_t** order, int32_t** gdesc, int32_t** ngroups);
-int launch_group(const Shape& s, const int32_t* sel, int32_t* order, int32_t* gdesc, int32_t* ngroups,
-                 cudaStream_t st);
+void carve_group_workspace(const Shape& s, void* ws, int32_t** order, int32_t** gdesc, int32_t** ngroups,
+                           GroupRec** recs);
+int launch_group(const Shape& s, const int32_t* sel, const GroupArgs& ga, int32_t* order, int32_t* gdesc,
+                 int32_t* ngroups, GroupRec* recs, cudaStream_t st);
 bool fwd_grp_supported(const Shape& s);
-int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* order, const int32_t* gdesc,
-                   const int32_t* ngroups, cudaStream_t st);
+int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* ngroups, const GroupRec* recs,
+                   cudaStream_t st);
 
 // tensor-core kernels (bf16, B = 16, d in {64, 128}, K_1 in {8, 16})
 bool fwd_tc_supported(const Shape& s);

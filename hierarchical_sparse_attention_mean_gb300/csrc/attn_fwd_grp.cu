@@ -31,8 +31,8 @@
 //
 // Warp roles (persistent CTAs, groups strided over CTAs, alternate groups to
 // the two softmax warpgroups):
-//   warps 0, 2  one per softmax warpgroup: its groups' set-up (query blocks,
-//               union, masks), Q boxes, pooled K/V rows (cp.async), K and V
+//   warps 0, 2  one per softmax warpgroup: its groups' records (group.cu)
+//               into the Q slots, Q boxes, pooled K/V rows (cp.async), K and V
 //               boxes of the tiles;
 //   warps 1, 3  MMA issuers, one per softmax warpgroup (warp 1 also owns TMEM);
 //   warps 4-7,  softmax / epilogue warpgroups, each with two S and two P
@@ -75,15 +75,6 @@ struct GCfg {
     static constexpr int TM_S = 0, TM_P = 128, TM_O = 192, TM_WG = 256;
 };
 
-template <int K1>
-struct GMeta {
-    uint32_t mask[8][GCfg<K1>::MW];  // bit u: union block u selected by query block q
-    int uni[GCfg<K1>::NU];           // union blocks, ascending
-    int qb[8];                       // the group's query blocks
-    int count, nslots;
-    long long slice;
-};
-
 struct GBar {
     uint64_t q_full[4], q_empty[4], k_full[6], k_empty[6], v_full[6], v_empty[6];
     uint64_t s_full[2][2], s_free[2][2], p_full[2][2], pv_done[2][2], o_free[2], drain[2];
@@ -94,13 +85,14 @@ struct GBar {
 
 struct GArgs {
     AttnArgs a;
-    const int32_t *order, *gdesc, *ngroups;  // grouping (group.cu), per window of query blocks
-    int windows, win;                          // windows per slice, query blocks per window
+    const int32_t* ngroups;  // groups per window of query blocks (group.cu)
+    const GroupRec* recs;    // group records, at slice * T + window * win + group
+    int windows, win;        // windows per slice, query blocks per window
 };
 
 __device__ __forceinline__ bool wait_all(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status,
                                          int limit) {
-    const bool ok = mbar_wait(mbar, parity, abort_flag, status, limit);
+    const bool ok = mbar_wait_n(mbar, parity, abort_flag, status, limit);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -178,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                const __grid_constant__ CUtensorMap mv, GArgs ga) {
     using C = GCfg<K1>;
-    using Meta = GMeta<K1>;
+    using Meta = GroupRec;
     constexpr int D = C::D;
     const AttnArgs& a = ga.a;
     extern __shared__ unsigned char smem_raw[];
@@ -243,20 +235,11 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
         int cur_win = 0;
         long long qissued = 0;                  // groups whose Q slot copies were issued
         constexpr int R = C::NU / 32;
-        // The next group's description is loaded one group ahead: its query
-        // blocks (lane < count), selection entries (value << 3 | query block;
-        // element r * 32 + lane) and enrichment tokens (lane = query block *
-        // kLeMax + level), so that these dependent loads overlap the current
-        // group's copies.
-        long long n_slice = 0;
-        int n_count = 0, n_qb = -1, n_ce = 0;
-        int n_v[R];
+        // The next group's record (group.cu) is loaded one group ahead, one
+        // independent 16-byte piece per lane, so the load is in flight while
+        // this group's tiles go out.
+        uint4 n_rec = make_uint4(0u, 0u, 0u, 0u);
         auto load_next = [&](long long jn) {
-            n_count = 0;
-            n_qb = -1;
-            n_ce = 0;
-#pragma unroll
-            for (int r = 0; r < R; r++) n_v[r] = 0x7FFFFFFF;
             if (jn >= mineW[w]) return;
             const long long gi = blockIdx.x + (2 * jn + w) * G;
             while (cur_slice < a.slices && gi >= cur_base + ga.ngroups[cur_slice * ga.windows + cur_win]) {
@@ -266,121 +249,39 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
                     cur_slice++;
                 }
             }
-            n_slice = cur_slice;
-            const int gd = ga.gdesc[n_slice * T + cur_win * ga.win + (int)(gi - cur_base)];
-            const int start = gd & 0xFFFF;
-            n_count = gd >> 16;
-            n_qb = lane < n_count ? ga.order[n_slice * T + start + lane] : -1;
-#pragma unroll
-            for (int r = 0; r < R; r++) {
-                const int e = r * 32 + lane, qs = e / K1, c = e % K1;
-                const int qb = __shfl_sync(0xffffffffu, n_qb, qs & 7);
-                if (qs < n_count) {
-                    int jb = a.sel[(n_slice * T + qb) * a.K1 + c];
-                    if (jb < 0 || jb >= T) {
-                        set_status(a.status, LLSA_ERR_BAD_INDEX);
-                        jb = 0;
-                    }
-                    n_v[r] = (jb << 3) | qs;
-                }
-            }
-            {
-                const int qs = lane / kLeMax, l = lane % kLeMax;
-                const int qb = __shfl_sync(0xffffffffu, n_qb, qs & 7);
-                if (qs < n_count && l < Le) {
-                    int e = a.coarse[(n_slice * T + qb) * a.C + a.col_off[l + 1]];
-                    if (e < 0 || e >= a.lv.n_level[l + 1]) {
-                        set_status(a.status, LLSA_ERR_BAD_INDEX);
-                        e = 0;
-                    }
-                    n_ce = e;
-                }
-            }
+            const GroupRec* rec = ga.recs + cur_slice * T + cur_win * ga.win + (int)(gi - cur_base);
+            n_rec = reinterpret_cast<const uint4*>(rec)[lane];
         };
         load_next(0);
-        // Set-up of group jn in its Q slot (free by now): union, masks and
-        // description, Q boxes, pooled rows; then the next description.
+        // Set-up of group jn in its Q slot (free by now): the record into the
+        // slot, Q boxes, pooled rows; then the next record.
         auto setup = [&](long long jn) {
             const int qsl = w * C::NQW + (int)(jn % C::NQW);
             unsigned char* slot = qslots + qsl * C::QSLOT;
             Meta* meta = reinterpret_cast<Meta*>(slot + C::META_OFF);
-            const long long slice = n_slice;
-            const int count = n_count, qb_l = n_qb, ce_l = n_ce;
-            int v[R];
-#pragma unroll
-            for (int r = 0; r < R; r++) v[r] = n_v[r];
-            // bitonic sort of the R * 32 entries (element r * 32 + lane)
-#pragma unroll
-            for (int kk = 2; kk <= R * 32; kk <<= 1)
-#pragma unroll
-                for (int jj = kk >> 1; jj > 0; jj >>= 1) {
-                    if (jj >= 32) {
-                        const int rj = jj >> 5;
-#pragma unroll
-                        for (int r = 0; r < R; r++)
-                            if ((r & rj) == 0) {
-                                const bool up = ((r * 32 + lane) & kk) == 0;
-                                const int x = v[r], y = v[r + rj];
-                                if ((x > y) == up) {
-                                    v[r] = y;
-                                    v[r + rj] = x;
-                                }
-                            }
-                    } else {
-#pragma unroll
-                        for (int r = 0; r < R; r++) {
-                            const int y = __shfl_xor_sync(0xffffffffu, v[r], jj);
-                            const bool lower = (lane & jj) == 0;
-                            const bool up = ((r * 32 + lane) & kk) == 0;
-                            const int mn = min(v[r], y), mx = max(v[r], y);
-                            v[r] = (lower == up) ? mn : mx;  // ascending pairs keep the min below
-                        }
-                    }
-                }
-            // union slots: the first entry of each run of equal blocks
-            for (int x = lane; x < 8 * C::MW; x += 32) (&meta->mask[0][0])[x] = 0u;
+            reinterpret_cast<uint4*>(meta)[lane] = n_rec;
             __syncwarp();
-            int base = 0;
-#pragma unroll
-            for (int r = 0; r < R; r++) {
-                int prev = __shfl_up_sync(0xffffffffu, v[r], 1);
-                const int last_prev = __shfl_sync(0xffffffffu, v[r > 0 ? r - 1 : 0], 31);
-                if (lane == 0) prev = r > 0 ? last_prev : -1;
-                const bool valid = v[r] != 0x7FFFFFFF;
-                const bool first = valid && (prev < 0 || (prev >> 3) != (v[r] >> 3));
-                const unsigned fm = __ballot_sync(0xffffffffu, first);
-                const int slot_id = base + __popc(fm & (0xFFFFFFFFu >> (31 - lane))) - 1;
-                if (first) meta->uni[slot_id] = v[r] >> 3;
-                if (valid) atomicOr(&meta->mask[v[r] & 7][slot_id >> 5], 1u << (slot_id & 31));
-                base += __popc(fm);
-            }
-            const int nslots = base;
-            if (lane < 8) meta->qb[lane] = qb_l;
-            if (lane == 0) {
-                meta->count = count;
-                meta->nslots = nslots;
-                meta->slice = slice;
-            }
-            __syncwarp();
+            const int count = meta->count;
+            const long long slice = meta->slice;
+            const int qb_l = lane < count ? meta->qb[lane] : 0;
             // the slot's copies: Q rows (TMA), pooled K and V rows of the
             // group's enrichment tokens (cp.async, 16-byte pieces); the
-            // barrier's completion also publishes the description above
+            // barrier's completion also publishes the record to the consumers
             const uint32_t qf = smem_u32(&bar->q_full[qsl]);
             if (lane == 0) mbar_arrive_expect_tx(qf, (uint32_t)(count * 16 * D * 2));
             __syncwarp();
             if (lane < count)
                 tma_load_2d(smem_u32(slot + lane * 2048), &mq, 0, (int)(slice * a.n + (long long)qb_l * 16), qf);
             {
-                // pooled K and V rows: lane-parallel 16-byte pieces, row index
-                // x = (query block * kLeMax + level) * 2 + (0: K, 1: V)
+                // row x = (query block * kLeMax + level) * 2 + (0: K, 1: V)
                 constexpr int per_row = D * 4 / 16;
                 const int items = count * kLeMax * 2 * per_row;
                 for (int it0 = 0; it0 < items; it0 += 32) {
                     const int it = it0 + lane;
                     const int row = it / per_row, piece = it % per_row;
-                    const int ql = row >> 1, isv = row & 1, l = ql % kLeMax;
-                    const int e = __shfl_sync(0xffffffffu, ce_l, ql & 31);
+                    const int ql = row >> 1, isv = row & 1, qs = ql / kLeMax, l = ql % kLeMax;
                     if (it >= items || l >= Le) continue;
+                    const int e = meta->ce[qs][l];
                     const float* src = (isv ? a.vpyr : a.kpyr) + slice * a.pyr_stride +
                                        (long long)(a.lv.row_offset[l + 1] + e) * D + piece * 4;
                     unsigned char* dst = slot + (isv ? C::PV_OFF : C::PK_OFF) + ql * D * 4 + piece * 16;
@@ -758,7 +659,7 @@ int launch_k(const Shape& s, const GArgs& ga, const CUtensorMap& mq, const CUten
              cudaStream_t st) {
     using C = GCfg<K1>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(sizeof(GMeta<K1>) <= 1024, "meta block");
+    static_assert(sizeof(GroupRec) <= 1024, "meta block");
     static_assert(sizeof(GBar) <= 1024, "barrier block");
     if (cudaFuncSetAttribute(fwd_grp_kernel<K1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
         return LLSA_ERR_CUDA;
@@ -776,8 +677,8 @@ bool fwd_grp_supported(const Shape& s) {
            s.Lc == s.Le && group_supported(s) && s.slices * (long long)s.n < (1LL << 31);
 }
 
-int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* order, const int32_t* gdesc,
-                   const int32_t* ngroups, cudaStream_t st) {
+int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* ngroups, const GroupRec* recs,
+                   cudaStream_t st) {
     CUtensorMap mq, mk, mv;
     const long long rows = s.slices * (long long)s.n;
     LLSA_TRY(make_tmap_bf16(&mq, a.q, rows, s.d, 16));
@@ -785,9 +686,8 @@ int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* order, cons
     LLSA_TRY(make_tmap_bf16(&mv, a.v, rows, s.d, 16));
     GArgs ga;
     ga.a = a;
-    ga.order = order;
-    ga.gdesc = gdesc;
     ga.ngroups = ngroups;
+    ga.recs = recs;
     ga.windows = group_windows(s);
     ga.win = kGroupWindow;
     return s.K1 == 8 ? launch_k<8>(s, ga, mq, mk, mv, st) : launch_k<16>(s, ga, mq, mk, mv, st);

@@ -12,6 +12,8 @@
 #include <initializer_list>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "internal.h"
 
 namespace llsa {
@@ -46,8 +48,19 @@ int scratch_on_current_device(int32_t** out) {
 
 using namespace llsa;
 
+static int noalloc_transpose(const llsa_params* p, const int32_t* sel_idx, int32_t* col_ptr, int32_t* row_idx,
+                             void* stream);
+
 extern "C" int llsa_index_transpose_noalloc(const llsa_params* p, const int32_t* sel_idx, int32_t* col_ptr,
                                             int32_t* row_idx, void* stream) {
+    nvtxRangePushA("llsa_index_transpose_noalloc");
+    const int rc = noalloc_transpose(p, sel_idx, col_ptr, row_idx, stream);
+    nvtxRangePop();
+    return rc;
+}
+
+static int noalloc_transpose(const llsa_params* p, const int32_t* sel_idx, int32_t* col_ptr, int32_t* row_idx,
+                             void* stream) {
     llsa_sizes z;
     LLSA_TRY(llsa_get_sizes(p, &z));
     if (z.slices == 0) return LLSA_OK;

@@ -104,16 +104,36 @@ __device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase of the given parity to complete. Gives up after
-// `limit` polls (the library's wait limit, kSpinLimit unless a test lowered
-// it), or as soon as another thread of the CTA gave up (abort flag),
-// recording LLSA_ERR_TIMEOUT; returns false then.
+// Waits for the phase of the given parity to complete. Gives up, recording
+// LLSA_ERR_TIMEOUT, after `limit` polls (the library's wait limit: kSpinLimit
+// unless a failure-detection test lowered it), or as soon as another thread
+// of the CTA gave up (abort flag); returns false then. The loop bound is the
+// compile-time kSpinLimit and `limit` is read only on the failing path, which
+// keeps the waiting code of the hot loops as it compiles without a test limit.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status,
                                           int limit) {
-    if (*abort_flag) return false;
+    for (int it = 0; it < kSpinLimit; it++) {
+        if (mbar_try(mbar, parity)) return true;
+        if ((it & 7) == 7 && (*abort_flag || it >= limit)) {
+            if (!*abort_flag) {
+                *abort_flag = 1;
+                set_status(status, LLSA_ERR_TIMEOUT);
+            }
+            return false;
+        }
+    }
+    *abort_flag = 1;
+    set_status(status, LLSA_ERR_TIMEOUT);
+    return false;
+}
+
+// The same wait with the poll count itself as the loop bound (the grouped
+// forward kernel's waits compile better this way).
+__device__ __forceinline__ bool mbar_wait_n(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status,
+                                            int limit) {
     for (int it = 0; it < limit; it++) {
         if (mbar_try(mbar, parity)) return true;
-        if ((it & 63) == 63 && *abort_flag) return false;
+        if ((it & 7) == 7 && *abort_flag) return false;
     }
     *abort_flag = 1;
     set_status(status, LLSA_ERR_TIMEOUT);

@@ -60,10 +60,29 @@ def read_groups(b, slices, T):
     windows = (T + WIN - 1) // WIN
     ws = b.ws_f.view(torch.int32).cpu().numpy()
     a = ((4 * slices * T + 255) // 256) * 256 // 4
+    c = ((4 * slices * windows + 255) // 256) * 256 // 4
     order = ws[:slices * T].reshape(slices, T)
     gdesc = ws[a:a + slices * T].reshape(slices, T)
     ngroups = ws[2 * a:2 * a + slices * windows].reshape(slices, windows)
-    return order, gdesc, ngroups
+    recs = ws[2 * a + c:2 * a + c + slices * T * 128].reshape(slices, T, 128)  # 512-byte records
+    return order, gdesc, ngroups, recs
+
+
+def check_record(rec, members, sel_rows, coarse_rows, Le, sl):
+    """A group record: mask words [8][4], union (uint16 [128]), query blocks
+    (uint16 [8]), enrichment tokens (uint16 [8][4]), count, union size, slice."""
+    mask = rec[:32].view(np.uint32).reshape(8, 4)
+    u16 = rec[32:].view(np.uint16)
+    uni, qb, ce = u16[:128], u16[128:136], u16[136:168].reshape(8, 4)
+    count, nslots, slice_ = rec[116], rec[117], rec[118]
+    union = np.unique(sel_rows[members])
+    assert count == len(members) and slice_ == sl and nslots == len(union)
+    np.testing.assert_array_equal(uni[:nslots], union)
+    np.testing.assert_array_equal(qb[:count], members)
+    for q, m in enumerate(members):
+        bits = [(int(mask[q, u >> 5]) >> (u & 31)) & 1 for u in range(nslots)]
+        assert [union[u] for u in range(nslots) if bits[u]] == sorted(sel_rows[m].tolist())
+        np.testing.assert_array_equal(ce[q, :Le], coarse_rows[m, :Le])
 
 
 @pytest.mark.parametrize("name", ["llsa-fwd-n4096-d64-b2h8-K8-bf16", "grf-64x64-K16", "n65536-grf-2heads"])
@@ -82,8 +101,9 @@ def test_grouping_rule_and_partition(name):
     assert llsa.llsa_get_status() == 0
     s = llsa.get_sizes(p)
     T = s.n_blocks
-    order, gdesc, ngroups = read_groups(b, s.slices, T)
+    order, gdesc, ngroups, recs = read_groups(b, s.slices, T)
     sel = b.sel_idx.cpu().numpy()
+    coarse = b.coarse_idx.cpu().numpy()
     sizes = []
     for sl in range(s.slices):
         covered = []
@@ -95,6 +115,9 @@ def test_grouping_rule_and_partition(name):
             assert got == ref_groups
             covered += [order[sl][a0:a0 + c] for a0, c in got]
             sizes += [c for _, c in got]
+            for k, (a0, c) in enumerate(got):
+                if k % 7 == 0:   # a sample of the records
+                    check_record(recs[sl, w0 + k], order[sl][a0:a0 + c], sel[sl], coarse[sl], s.enrich_levels, sl)
         assert sorted(np.concatenate(covered).tolist()) == list(range(T))   # a partition
     if w.kind == "grf":
         # spatially structured selections group well (several blocks per group)
