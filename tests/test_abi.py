@@ -127,7 +127,6 @@ def test_workspace_sizes(lib):
     assert llsa.workspace_bytes(p, llsa.OP_TRANSPOSE) == 12 * 4096 * 4
     assert llsa.workspace_bytes(p, llsa.OP_BWD) > 12 * 65536 * 4
     # the grouping of query blocks: order and group list per slice, group
-    # counts per window of 1024 query blocks
     # counts per window of 1024 query blocks, and a 512-byte record per group
     assert llsa.workspace_bytes(p, llsa.OP_FWD) == 2 * 12 * 4096 * 4 + 256 + 12 * 4096 * 512
     # shapes the grouped forward does not take need no forward workspace
