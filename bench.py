@@ -343,9 +343,44 @@ def run_llsa(args, ws, rank, local):
         if ws > 1:
             torch.distributed.barrier()
 
-    # ---- timed region: K device-resident steps
+    # ---- per-kernel durations, from a profiled pass before the timed region:
+    # events recorded between kernels keep each launch from overlapping the
+    # drain of the one before, so the timed region brackets only the
+    # dominant kernel with events
+    n_prof = max(3, min(args.steps, 10))
+    llsa.profile_reset()
+    llsa.profile_only(None)
+    llsa.profile_enable(True)
+    for _ in range(n_prof):
+        step()
+    torch.cuda.synchronize()
+    llsa.profile_enable(False)
+    records = llsa.profile_read(cap=64 * n_prof + 64)
+    per = {}
+    for name, ms in records:
+        k = kernel_key(name)
+        tot, cnt = per.get(k, (0.0, 0))
+        per[k] = (tot + ms, cnt + 1)
+    stage_ms = {k: round(t / n_prof, 4) for k, (t, c) in per.items()}
+    stage_each = {}  # stage -> per-step sums (every step launches the same kernels in order)
+    if len(records) % n_prof == 0:
+        per_step = len(records) // n_prof
+        for k in range(n_prof):
+            sums = {}
+            for name, ms in records[k * per_step:(k + 1) * per_step]:
+                key = kernel_key(name)
+                sums[key] = sums.get(key, 0.0) + ms
+            for key, v in sums.items():
+                stage_each.setdefault(key, []).append(v)
+    dom = max(per, key=lambda k: per[k][0])
+    dom_names = sorted({name for name, _ in records if kernel_key(name) == dom})
+    tensor_path = dom in llsa_tensor_kernels(records)
+
+    # ---- timed region: K device-resident steps, events around the dominant
+    # kernel's launches only
     sampler = ClockSampler(torch.cuda.current_device())
     llsa.profile_reset()
+    llsa.profile_only(dom_names[0] if len(dom_names) == 1 else None)
     llsa.profile_enable(True)
     sampler.start()
     barrier()
@@ -364,33 +399,15 @@ def run_llsa(args, ws, rank, local):
     clocks = sampler.stop()
     launches = llsa.llsa_launch_count() - launches0
     llsa.profile_enable(False)
-    records = llsa.profile_read(cap=64 * args.steps + 64)
+    llsa.profile_only(None)
+    timed = [ms for name, ms in llsa.profile_read(cap=64 * args.steps + 64) if kernel_key(name) == dom]
     elapsed = max_over_ranks(e0.elapsed_time(e1), ws, dev)
     ms_step = elapsed / args.steps
-
-    # per-kernel durations from the events recorded around each launch
-    per = {}
-    for name, ms in records:
-        k = kernel_key(name)
-        tot, cnt = per.get(k, (0.0, 0))
-        per[k] = (tot + ms, cnt + 1)
-    stage_ms = {k: round(t / args.steps, 4) for k, (t, c) in per.items()}
     step_each = [marks[k].elapsed_time(marks[k + 1]) for k in range(args.steps)]
-    stage_each = {}  # stage -> per-step sums (every step launches the same kernels in order)
-    if args.steps > 0 and len(records) % args.steps == 0:
-        per_step = len(records) // args.steps
-        for k in range(args.steps):
-            sums = {}
-            for name, ms in records[k * per_step:(k + 1) * per_step]:
-                key = kernel_key(name)
-                sums[key] = sums.get(key, 0.0) + ms
-            for key, v in sums.items():
-                stage_each.setdefault(key, []).append(v)
     peaks, peak_src = load_peaks()
     work = work_model(w, s)
-    dom = max(per, key=lambda k: per[k][0])
-    avg_ms = per[dom][0] / per[dom][1]
-    tensor_path = dom in llsa_tensor_kernels(records)
+    # the dominant kernel's duration, live in the timed region
+    avg_ms = sum(timed) / len(timed) if timed else per[dom][0] / per[dom][1]
     roof = kernel_bound(dom, avg_ms, work, peaks, tensor_path)
     traffic = args.traffic if args.traffic is not None else recorded_traffic(w.name, dom)
     roof.update({"kernel": dom, "avg_launch_ms": round(avg_ms, 4), "peak_source": peak_src,
@@ -468,6 +485,7 @@ def run_llsa(args, ws, rank, local):
                    "flops_per_step": work["step_flops"], "flops_counted": "14*d per (query, key) pair: "
                    "fwd 4d, bwd 10d (S, dP, dV, dK, dQ); selection excluded"},
         "stage_ms": stage_ms,
+        "stage_ms_from": f"{n_prof} profiled steps before the timed region (events around every launch)",
         "spread_ms": {"step": spread(step_each), **{k: spread(v) for k, v in stage_each.items()}},
         "stage_gbs": stage_gbs,
         "roofline": roof,

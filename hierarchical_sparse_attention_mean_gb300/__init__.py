@@ -87,6 +87,7 @@ def _load():
     lib.llsa_launch_count.restype = ctypes.c_ulonglong
     lib.llsa_test_set_wait_limit.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.llsa_profile_enable.argtypes = [ctypes.c_int]
+    lib.llsa_profile_only.argtypes = [ctypes.c_char_p]
     lib.llsa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float), ctypes.c_int]
     _lib = lib
     return lib
@@ -301,6 +302,11 @@ def profile_enable(on: bool = True):
 
 def profile_reset():
     _load().llsa_profile_reset()
+
+
+def profile_only(prefix: str | None = None):
+    """Time only kernels whose name starts with `prefix` (None: all)."""
+    _load().llsa_profile_only(prefix.encode() if prefix else None)
 
 
 def profile_read(cap: int = 4096):

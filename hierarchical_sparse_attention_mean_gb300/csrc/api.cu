@@ -7,6 +7,7 @@
 #include <atomic>
 #include <initializer_list>
 #include <mutex>
+#include <string>
 #include <vector>
 
 #include <nvtx3/nvToolsExt.h>
@@ -35,6 +36,8 @@ struct ProfRecord {
     cudaEvent_t start, stop;
 };
 bool g_prof_on = false;
+std::string g_prof_prefix;            // record only launches whose name starts with it ("" : all)
+thread_local bool t_prof_open = false;  // launch_begin recorded a start event for this thread's launch
 std::vector<ProfRecord> g_prof;
 std::vector<cudaEvent_t> g_event_pool;
 
@@ -95,8 +98,11 @@ int sm_count() {
 }
 
 void launch_begin(const char* name, cudaStream_t st) {
+    t_prof_open = false;
     if (!g_prof_on) return;
     std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_prof_prefix.empty() && strncmp(name, g_prof_prefix.c_str(), g_prof_prefix.size()) != 0) return;
+    t_prof_open = true;
     ProfRecord r{name, take_event(), take_event()};
     cudaEventRecord(r.start, st);
     g_prof.push_back(r);
@@ -105,9 +111,10 @@ void launch_begin(const char* name, cudaStream_t st) {
 int launch_end(const char* name, cudaStream_t st) {
     (void)name;
     g_launches.fetch_add(1, std::memory_order_relaxed);
-    if (g_prof_on) {
+    if (t_prof_open) {
         std::lock_guard<std::mutex> lk(g_mu);
         if (!g_prof.empty()) cudaEventRecord(g_prof.back().stop, st);
+        t_prof_open = false;
     }
     return cudaGetLastError() == cudaSuccess ? LLSA_OK : LLSA_ERR_CUDA;
 }
@@ -383,6 +390,12 @@ unsigned long long llsa_launch_count(void) { return g_launches.load(); }
 int llsa_profile_enable(int on) {
     std::lock_guard<std::mutex> lk(g_mu);
     g_prof_on = on != 0;
+    return LLSA_OK;
+}
+
+int llsa_profile_only(const char* prefix) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_prof_prefix = prefix ? prefix : "";
     return LLSA_OK;
 }
 

@@ -272,6 +272,13 @@ int llsa_profile_enable(int on);
 int llsa_profile_reset(void);
 int llsa_profile_read(const char **names, float *ms, int cap);
 
+/* Restricts the timing above to kernels whose name starts with `prefix` (the
+ * names llsa_profile_read reports); NULL or "" times every kernel again. The
+ * string is copied. Events recorded between kernels keep the GPU from
+ * starting the next kernel while the one before drains, so a timed run that
+ * needs one kernel's duration records only that kernel. Returns LLSA_OK. */
+int llsa_profile_only(const char *prefix);
+
 #ifdef __cplusplus
 }
 #endif
