@@ -339,6 +339,19 @@ class Buffers:
         self.ws_f = torch.empty(max(16, workspace_bytes(p, OP_FWD)), dtype=torch.uint8, device=dev)
         self.ws_t = torch.empty(max(16, workspace_bytes(p, OP_TRANSPOSE)), dtype=torch.uint8, device=dev)
         self.ws_b = torch.empty(max(16, workspace_bytes(p, OP_BWD)), dtype=torch.uint8, device=dev)
+        # the sparse-index transpose that forward() issues on a side stream
+        self._side = None          # that stream (made on first use)
+        self._sel_ready = None     # event: the selection it reads is written
+        self._transposed = None    # event: col_ptr / row_idx are written
+        self._pending = False      # a transpose was issued that backward() has not waited for
+
+    def side_stream(self):
+        import torch
+        if self._side is None:
+            self._side = torch.cuda.Stream(device=self.sel_idx.device)
+            self._sel_ready = torch.cuda.Event()
+            self._transposed = torch.cuda.Event()
+        return self._side
 
     def level(self, l: int):
         """I^(l) as [bh, n_l, K_l] (l >= 2) view of level_idx; I^(1) = sel_idx."""
@@ -349,22 +362,52 @@ class Buffers:
         return self.level_idx[:, off:off + s.n_level[l] * s.topk_level[l]].view(-1, s.n_level[l], s.topk_level[l])
 
 
+def _as_stream(stream, device):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
 def forward(p: Params, q, k, v, bufs: Buffers | None = None, stream=None) -> Buffers:
-    """pool -> select -> fwd. Returns the buffers (o, lse, indices, pyramids)."""
+    """pool -> select -> fwd. Returns the buffers (o, lse, indices, pyramids).
+
+    The sparse-index transpose that backward() needs depends on the selection
+    alone: it is issued here on a side stream, after select, so that it runs
+    beside the forward's grouping pass; backward() waits for it."""
     b = bufs or Buffers(p, q.device)
-    llsa_pool(p, q, k, v, b.pyr, stream=stream)
-    llsa_select(p, b.pyr, b.sel_idx, b.coarse_idx, b.level_idx, stream=stream)
-    llsa_fwd(p, q, k, v, b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse, b.ws_f, stream=stream)
+    st = _as_stream(stream, q.device)
+    if b._pending:
+        st.wait_event(b._transposed)  # the previous transpose still reads sel_idx
+    llsa_pool(p, q, k, v, b.pyr, stream=st)
+    llsa_select(p, b.pyr, b.sel_idx, b.coarse_idx, b.level_idx, stream=st)
+    side = b.side_stream()
+    b._sel_ready.record(st)
+    side.wait_event(b._sel_ready)
+    llsa_index_transpose(p, b.sel_idx, b.col_ptr, b.row_idx, b.ws_t, stream=side)
+    b._transposed.record(side)
+    b._pending = True
+    for t in (b.sel_idx, b.col_ptr, b.row_idx, b.ws_t):
+        t.record_stream(side)  # in use there until the transpose is done
+    llsa_fwd(p, q, k, v, b.pyr, b.sel_idx, b.coarse_idx, b.o, b.lse, b.ws_f, stream=st)
     return b
 
 
 def backward(p: Params, q, k, v, dout, b: Buffers, dq=None, dk=None, dv=None, stream=None):
-    """transpose -> bwd, after forward(). Returns (dq, dk, dv)."""
+    """bwd after forward() (and its index transpose). Returns (dq, dk, dv)."""
     import torch
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    llsa_index_transpose(p, b.sel_idx, b.col_ptr, b.row_idx, b.ws_t, stream=stream)
+    st = _as_stream(stream, q.device)
+    if b._pending:
+        st.wait_event(b._transposed)
+        b._pending = False
+    else:
+        llsa_index_transpose(p, b.sel_idx, b.col_ptr, b.row_idx, b.ws_t, stream=st)
+    stream = st
     llsa_bwd(p, q, k, v, b.o, b.lse, dout, b.pyr, b.sel_idx, b.coarse_idx, b.col_ptr, b.row_idx, dq, dk, dv,
              b.ws_b, stream=stream)
     return dq, dk, dv
