@@ -184,29 +184,40 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         // Item n uses stage n % STAGES for the (n / STAGES)-th time. The query
         // blocks of the next item are located while this one is issued.
         const int role = warp == 0 ? 0 : warp - 1;
+        // key block kb_walk is global block blockIdx.x + kb_walk * G, i.e.
+        // block w_j of slice w_slice (walked, no division per item)
         int kb_walk = 0;
-        auto locate = [&](int n, int& kb, int& nv, int& qb) {
-            while (kb_walk + 1 < n_kb && kitem[kb_walk + 1] <= n) kb_walk++;
+        long long w_slice = blockIdx.x / a.T;
+        int w_j = (int)(blockIdx.x - w_slice * a.T);
+        auto locate = [&](int n, int& kb, int& nv, int& qb, long long& ksl, int& kj) {
+            while (kb_walk + 1 < n_kb && kitem[kb_walk + 1] <= n) {
+                kb_walk++;
+                w_j += G;
+                while (w_j >= a.T) {
+                    w_j -= a.T;
+                    w_slice++;
+                }
+            }
             kb = kb_walk;
+            ksl = w_slice;
+            kj = w_j;
             const int gi = n - kitem[kb];
             nv = min(8, kcnt[kb] - 8 * gi);
-            qb = lane < nv ? a.row_idx[((long long)(blockIdx.x + (long long)kb * G) / a.T) * a.T * a.K1 + kbeg[kb] + 8 * gi + lane] : 0;
+            qb = lane < nv ? a.row_idx[w_slice * a.T * a.K1 + kbeg[kb] + 8 * gi + lane] : 0;
         };
-        int kb, nv, qb, kb1 = 0, nv1 = 0, qb1 = 0;
+        int kb, nv, qb, kb1 = 0, nv1 = 0, qb1 = 0, j, j1 = 0;
+        long long slice, slice1 = 0;
         int issued = -1;
-        if (n_items > 0) locate(0, kb1, nv1, qb1);
+        if (n_items > 0) locate(0, kb1, nv1, qb1, slice1, j1);
         const int ni = (a.test_flags & LLSA_TEST_NO_COPIES) ? 0 : n_items;  // failure-detection test
         for (int n = 0; n < ni; n++) {
-            kb = kb1; nv = nv1; qb = qb1;
-            if (n + 1 < n_items) locate(n + 1, kb1, nv1, qb1);
+            kb = kb1; nv = nv1; qb = qb1; slice = slice1; j = j1;
+            if (n + 1 < n_items) locate(n + 1, kb1, nv1, qb1, slice1, j1);
             const int st = n % C::STAGES, u = n / C::STAGES;
             bool ok = true;
             if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status, a.spin);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
-            const long long g = blockIdx.x + (long long)kb * G;
-            const long long slice = g / a.T;
-            const int j = (int)(g - slice * a.T);
             if (lane < nv && (qb < 0 || qb >= a.T)) {
                 set_status(a.status, LLSA_ERR_BAD_INDEX);
                 qb = 0;
@@ -384,21 +395,31 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         // (lse, D) of this thread's query row for one of the group's items,
         // loaded one item ahead of its use, so the two dependent loads (the
         // CSC row, then the pair) hide behind the item before
-        auto load_ld = [&](int kb2, int gi2) -> float2 {
+        auto load_ld = [&](int kb2, int gi2, long long sl2) -> float2 {
             if (kb2 >= n_kb || tq >= 16 * min(8, kcnt[kb2] - 8 * gi2)) return make_float2(0.f, 0.f);
-            const long long g2 = blockIdx.x + (long long)kb2 * G;
-            const long long sl2 = g2 / a.T;
             int qb2 = a.row_idx[sl2 * a.T * a.K1 + kbeg[kb2] + 8 * gi2 + (tq >> 4)];
             if (qb2 < 0 || qb2 >= a.T) qb2 = 0;  // reported by the gather warps
             return *reinterpret_cast<const float2*>(a.Dbuf + 2 * (sl2 * a.n + (long long)qb2 * 16 + (tq & 15)));
         };
+        // key block kb of this group is block j of slice `slice`, and its
+        // next item's key block kbn block nj of slice nsl (walked by 2 G)
+        const long long g0 = blockIdx.x + (long long)w * G;
+        long long slice = g0 / a.T, nsl = slice;
+        int j = (int)(g0 - slice * a.T), nj = j;
+        auto step2 = [&](long long& sl, int& jj) {
+            jj += 2 * G;
+            while (jj >= a.T) {
+                jj -= a.T;
+                sl++;
+            }
+        };
         int kbn = w, gin = 0;  // the group's next item
-        while (kbn < n_kb && kcnt[kbn] == 0) kbn += 2;
-        float2 ld_next = load_ld(kbn, gin);
-        for (int kb = w; kb < n_kb; kb += 2) {
-            const long long g = blockIdx.x + (long long)kb * G;
-            const long long slice = g / a.T;
-            const int j = (int)(g - slice * a.T);
+        while (kbn < n_kb && kcnt[kbn] == 0) {
+            kbn += 2;
+            step2(nsl, nj);
+        }
+        float2 ld_next = load_ld(kbn, gin, nsl);
+        for (int kb = w; kb < n_kb; kb += 2, step2(slice, j)) {
             const int cnt = kcnt[kb], items = (cnt + 7) / 8;
             // pooled-level gradients above this key block: loaded before its
             // items, combined only in its epilogue so the loads' latency hides
@@ -426,10 +447,12 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                     gin++;
                 } else {
                     gin = 0;
-                    do kbn += 2;
-                    while (kbn < n_kb && kcnt[kbn] == 0);
+                    do {
+                        kbn += 2;
+                        step2(nsl, nj);
+                    } while (kbn < n_kb && kcnt[kbn] == 0);
                 }
-                ld_next = load_ld(kbn, gin);
+                ld_next = load_ld(kbn, gin, nsl);
                 const float lse2 = ld.x * kLog2e, Dq = ld.y;
                 mbar_wait(smem_u32(&ms->s_full[w][b]), ph, abort_flag, a.status, a.spin);
                 tc_fence_after();

@@ -128,17 +128,23 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
         const int role = warp == 0 ? 0 : warp - 1;
         auto load_idx = [&](long long bl) -> int {
             if (bl >= mine) return 0;
-            const long long g = blockIdx.x + bl * G;
-            const long long slice = g / a.T;
-            const int i = (int)(g - slice * a.T);
-            if (role == 0) return lane < Le ? a.coarse[(slice * a.T + i) * a.C + lane] : 0;
-            return lane < K1 ? a.sel[(slice * a.T + i) * a.K1 + lane] : 0;
+            const long long g = blockIdx.x + bl * G;  // global query block (slice * T + i)
+            if (role == 0) return lane < Le ? a.coarse[g * a.C + lane] : 0;
+            return lane < K1 ? a.sel[g * a.K1 + lane] : 0;
         };
         const uint32_t my_bytes = role == 0 ? 3 * C::Q_BYTES + 64 + 2 * Le * D * 4 : C::KV_BYTES;
         int ix0 = load_idx(0), ix1 = load_idx(1);
         long long issued = -1;
         const long long nb = (a.test_flags & LLSA_TEST_NO_COPIES) ? 0 : mine;  // failure-detection test
-        for (long long bl = 0; bl < nb; bl++) {
+        // block bl is global query block blockIdx.x + bl * G: block i of
+        // slice `slice` (walked, no division per block)
+        long long slice = blockIdx.x / a.T;
+        int i = (int)(blockIdx.x - slice * a.T);
+        for (long long bl = 0; bl < nb; bl++, i += G) {
+            while (i >= a.T) {
+                i -= a.T;
+                slice++;
+            }
             int ix = ix0;
             ix0 = ix1;
             ix1 = load_idx(bl + 2);
@@ -147,9 +153,6 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if (u >= 1 && lane == 0) ok = mbar_wait(smem_u32(&ms->empty[st]), (u - 1) & 1, abort_flag, a.status, a.spin);
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0);
             if (!ok) break;
-            const long long g = blockIdx.x + bl * G;
-            const long long slice = g / a.T;
-            const int i = (int)(g - slice * a.T);
             unsigned char* sb = stages + st * C::STAGE_BYTES;
             const uint32_t fb = smem_u32(&ms->full[st]);
             if (lane == 0) mbar_arrive_expect_tx(fb, my_bytes);
@@ -303,9 +306,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             const long long g = blockIdx.x + bl * G;
             const uint32_t j = (uint32_t)(bl >> 1);
             const int st = (int)(bl % C::STAGES);
-            const long long slice = g / a.T;
-            const int i = (int)(g - slice * a.T);
-            const long long tok0 = slice * a.n + (long long)i * 16;
+            const long long tok0 = g * 16;  // slice * n + i * B (n = T * B)
             const unsigned char* sb = stages + st * C::STAGE_BYTES;
             const float* sKc = reinterpret_cast<const float*>(sb + C::OFF_C);
             const float* sLse = reinterpret_cast<const float*>(sb + C::OFF_L);
@@ -442,7 +443,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                     val = fmaf(g4.w, kc[3], val);
                     dst[c * D] = __float2bfloat16_rn(sc * val);
                 }
-                const long long off = (slice * a.T + i) * (long long)a.Le * D + dd;
+                const long long off = g * (long long)a.Le * D + dd;
 #pragma unroll
                 for (int l = 0; l < 4; l++)
                     if (l < Le) {
