@@ -190,7 +190,8 @@ def grouped_fwd_blocks(b, s, window: int = 1024):
     """Key blocks the grouped tensor-core forward gathers in one step: for
     every group of query blocks (read back from the forward's workspace), the
     size of the union of their selections. None when the forward took no
-    workspace (no grouping)."""
+    workspace (no grouping) or the per-query-block forward took the call
+    (groups of fewer than 4.5 query blocks on average, the library's rule)."""
     import numpy as np
     import torch
     T, slices = s.n_blocks, s.slices
@@ -202,6 +203,8 @@ def grouped_fwd_blocks(b, s, window: int = 1024):
     order = ws[:slices * T].reshape(slices, T)
     gdesc = ws[a:a + slices * T].reshape(slices, T)
     ngroups = ws[2 * a:2 * a + slices * windows].reshape(slices, windows)
+    if 2 * slices * T < 9 * int(ngroups.sum()):
+        return None
     sel = b.sel_idx.cpu().numpy().astype(np.int64)
     total = 0
     for sl in range(slices):
@@ -670,7 +673,7 @@ def run_sweep(args):
 
 
 def llsa_tensor_kernels(records):
-    return {kernel_key(n) for n, _ in records if n.endswith("_tc")}
+    return {kernel_key(n) for n, _ in records if n.endswith("_tc") or n.startswith("fwd_grp")}
 
 
 def cpu_baseline(w, x, s):

@@ -283,12 +283,15 @@ def llsa_get_status(stream=None) -> int:
 
 
 LLSA_TEST_NO_COPIES = 1
+LLSA_TEST_FORCE_GROUPED = 2
+LLSA_TEST_FORCE_PER_BLOCK = 4
 
 
 def test_set_wait_limit(polls: int = 0, flags: int = 0):
-    """Failure-detection test hook (llsa_test_set_wait_limit): polls before a
-    bounded device wait gives up (0: the kernels' own limit) and test
-    switches (LLSA_TEST_NO_COPIES: the copy warps issue nothing)."""
+    """Test hook (llsa_test_set_wait_limit): polls before a bounded device wait
+    gives up (0: the kernels' own limit) and test switches
+    (LLSA_TEST_NO_COPIES: the copy warps issue nothing; LLSA_TEST_FORCE_GROUPED
+    / LLSA_TEST_FORCE_PER_BLOCK: which tensor-core forward llsa_fwd takes)."""
     _check(_load().llsa_test_set_wait_limit(int(polls), int(flags)), "llsa_test_set_wait_limit")
 
 

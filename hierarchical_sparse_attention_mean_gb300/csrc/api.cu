@@ -212,7 +212,8 @@ using namespace llsa;
 extern "C" {
 
 int llsa_test_set_wait_limit(int polls, int flags) {
-    if (flags & ~LLSA_TEST_NO_COPIES) return LLSA_ERR_INVALID_ARG;
+    if (flags & ~(LLSA_TEST_NO_COPIES | LLSA_TEST_FORCE_GROUPED | LLSA_TEST_FORCE_PER_BLOCK)) return LLSA_ERR_INVALID_ARG;
+    if ((flags & LLSA_TEST_FORCE_GROUPED) && (flags & LLSA_TEST_FORCE_PER_BLOCK)) return LLSA_ERR_INVALID_ARG;
     g_wait_limit.store(polls > 0 ? polls : 0);
     g_test_flags.store(flags);
     return LLSA_OK;

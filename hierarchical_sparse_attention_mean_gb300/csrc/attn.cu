@@ -26,7 +26,12 @@ int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, cons
             g.n_level[l] = l < s.Le ? s.n_level[l + 1] : 1;
         }
         LLSA_TRY(launch_group(s, sel_idx, g, order, gdesc, ngroups, recs, st));
-        return launch_fwd_grp(s, a, ngroups, recs, st);
+        // both forwards are launched; each reads the group counts and only one
+        // does the work (the other returns at once)
+        LLSA_TRY(launch_fwd_grp(s, a, ngroups, recs, st));
+        a.ngroups = ngroups;
+        a.ngroups_n = s.slices * (long long)group_windows(s);
+        return launch_fwd_tc(s, a, st);
     }
     if (fwd_tc_supported(s)) return launch_fwd_tc(s, a, st);
     return launch_fwd_simt(s, a, st);

@@ -23,6 +23,10 @@ struct AttnArgs {
     int* status;
     int spin;        // polls before a bounded wait gives up (kSpinLimit unless a test lowered it)
     int test_flags;  // LLSA_TEST_* switches of llsa_test_set_wait_limit (0 in normal use)
+    // set when the grouping pass ran: its group counts per window (the
+    // forwards choose between them from these), else nullptr
+    const int32_t* ngroups;
+    long long ngroups_n;
     int rule;  // enrichment rule
     // enrichment columns: C per coarse row, Lc used (levels 1..Le); column c
     // holds a token of level col_level[c]; level l owns columns
@@ -77,6 +81,27 @@ void carve_group_workspace(const Shape& s, void* ws, int32_t** order, int32_t** 
 int launch_group(const Shape& s, const int32_t* sel, const GroupArgs& ga, int32_t* order, int32_t* gdesc,
                  int32_t* ngroups, GroupRec* recs, cudaStream_t st);
 bool fwd_grp_supported(const Shape& s);
+
+// Which forward runs after the grouping pass. The grouped forward costs about
+// four per-query-block forwards per group (measured on GB300 over inputs
+// whose groups average 1.9 to 5.5 query blocks), so it runs when the groups
+// hold at least 4.5 query blocks on average, unless a test forces one path.
+#ifdef __CUDACC__
+__device__ __forceinline__ bool grouped_forward(long long groups, long long blocks, int test_flags) {
+    if (test_flags & LLSA_TEST_FORCE_GROUPED) return true;
+    if (test_flags & LLSA_TEST_FORCE_PER_BLOCK) return false;
+    return 2 * blocks >= 9 * groups;
+}
+
+// Sum of n group counts, by one whole warp (every lane gets it).
+__device__ __forceinline__ long long sum_groups(const int32_t* ngroups, long long n, int lane) {
+    long long tot = 0;
+    for (long long u = lane; u < n; u += 32) tot += ngroups[u];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    return tot;
+}
+#endif
 int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* ngroups, const GroupRec* recs,
                    cudaStream_t st);
 

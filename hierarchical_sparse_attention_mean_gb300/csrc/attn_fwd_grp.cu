@@ -222,7 +222,10 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tbase = bar->tmem_slot;
     const long long total = bar->total_groups;
-    const long long mine = total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
+    // the per-query-block forward, launched after this one, takes the call
+    // when the groups are too small
+    const bool run = grouped_forward(total, a.slices * (long long)T, a.test_flags);
+    const long long mine = run && total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
     // groups of warpgroup w: the CTA's groups w, w + 2, ...
     const long long mineW[2] = {(mine + 1) / 2, mine / 2};
 

@@ -97,6 +97,15 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const long long total = a.slices * (long long)a.T;
     const int G = gridDim.x;
     const int K1 = NT * 8, Le = a.Le;
+    // after a grouping pass, the grouped forward may take this call instead
+    if (a.ngroups != nullptr) {
+        bool skip = false;
+        if (warp == 0) {
+            const long long groups = sum_groups(a.ngroups, a.ngroups_n, lane);
+            skip = lane == 0 && grouped_forward(groups, total, a.test_flags);
+        }
+        if (__syncthreads_or(skip)) return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; s++) {
@@ -515,6 +524,15 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     const long long total = a.slices * (long long)a.T;
     const int G = gridDim.x;
     const int K1 = NT * 8, Le = a.Le;
+    // after a grouping pass, the grouped forward may take this call instead
+    if (a.ngroups != nullptr) {
+        bool skip = false;
+        if (warp == 0) {
+            const long long groups = sum_groups(a.ngroups, a.ngroups_n, lane);
+            skip = lane == 0 && grouped_forward(groups, total, a.test_flags);
+        }
+        if (__syncthreads_or(skip)) return;
+    }
     const long long mine = total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
 
     if (threadIdx.x == 0) {

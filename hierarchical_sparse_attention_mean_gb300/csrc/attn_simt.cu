@@ -607,6 +607,8 @@ AttnArgs make_attn_args(const Shape& s) {
     a.status = status_ptr();
     a.spin = wait_limit();
     a.test_flags = test_flags();
+    a.ngroups = nullptr;
+    a.ngroups_n = 0;
     a.rule = s.rule;
     a.C = s.C;
     a.Lc = s.Lc;

@@ -188,17 +188,27 @@ int llsa_bwd(const llsa_params *p, const void *q, const void *k, const void *v, 
              const int32_t *coarse_idx, const int32_t *col_ptr, const int32_t *row_idx,
              void *dq, void *dk, void *dv, void *ws, size_t ws_bytes, void *stream);
 
-/* Test hook for failure detection; no counterpart in the paper. Sets how many
- * polls a bounded device wait of the tensor-core kernels makes before it gives
- * up and records LLSA_ERR_TIMEOUT in the status word (polls <= 0 restores the
- * kernels' own limit, about a second of polling), and test switches:
- *   LLSA_TEST_NO_COPIES  the kernels' copy warps issue no copies, so every
- *                        consumer's first wait runs out with no copy or MMA in
- *                        flight; the kernel then drains, frees its tensor
- *                        memory and exits, leaving its outputs undefined.
+/* Test hook; no counterpart in the paper. Sets how many polls a bounded
+ * device wait of the tensor-core kernels makes before it gives up and records
+ * LLSA_ERR_TIMEOUT in the status word (polls <= 0 restores the kernels' own
+ * limit, about a second of polling), and test switches:
+ *   LLSA_TEST_NO_COPIES        the kernels' copy warps issue no copies, so
+ *                              every consumer's first wait runs out with no
+ *                              copy or MMA in flight; the kernel then drains,
+ *                              frees its tensor memory and exits, leaving its
+ *                              outputs undefined (failure detection).
+ *   LLSA_TEST_FORCE_GROUPED    llsa_fwd takes the grouped tensor-core forward
+ *   LLSA_TEST_FORCE_PER_BLOCK  or the per-query-block one, whatever the
+ *                              grouping found (normally the grouped forward
+ *                              runs when its groups hold at least 4.5 query
+ *                              blocks on average); results agree either way
+ *                              within rounding.
  * Process-wide; applies to calls made after it; (0, 0) is the default state.
- * Host-side only, no device work. Unknown flag bits: LLSA_ERR_INVALID_ARG. */
+ * Host-side only, no device work. Unknown flag bits, or both FORCE bits:
+ * LLSA_ERR_INVALID_ARG. */
 #define LLSA_TEST_NO_COPIES 1
+#define LLSA_TEST_FORCE_GROUPED 2
+#define LLSA_TEST_FORCE_PER_BLOCK 4
 int llsa_test_set_wait_limit(int polls, int flags);
 
 /* Sparse index transpose for callers that cannot allocate device memory.

@@ -133,3 +133,12 @@ def test_workspace_sizes(lib):
     assert llsa.workspace_bytes(llsa.Params(1, 2, 4096, 128, topk=16), llsa.OP_FWD) == 0
     assert llsa.workspace_bytes(llsa.Params(1, 2, 1024, 64, dtype="fp32"), llsa.OP_FWD) == 0
     assert llsa.strerror(-9) == "device wait timed out"
+
+
+def test_test_hook_flags(lib):
+    assert lib.llsa_test_set_wait_limit(0, 8) == -1  # no such switch
+    both = llsa.LLSA_TEST_FORCE_GROUPED | llsa.LLSA_TEST_FORCE_PER_BLOCK
+    assert lib.llsa_test_set_wait_limit(0, both) == -1
+    for f in (llsa.LLSA_TEST_FORCE_GROUPED, llsa.LLSA_TEST_FORCE_PER_BLOCK, llsa.LLSA_TEST_NO_COPIES, 0):
+        assert lib.llsa_test_set_wait_limit(0, f) == 0
+    assert lib.llsa_test_set_wait_limit(0, 0) == 0

@@ -80,10 +80,33 @@ def test_select(case_data, name):
     assert total <= max(1, 0.01 * w.bh * (w.n // w.block)), total
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_fwd_with_oracle_indices(case_data, name):
+# the cases that can take the grouped tensor-core forward (bf16, d = 64,
+# B = 16, K_1 in {8, 16}): their forward is checked on both tensor-core paths
+# as well as on the one llsa_fwd picks
+GROUPABLE = [n for n, w in CASES.items() if w.dtype == "bf16" and w.d == 64 and w.block == 16 and w.topk in (8, 16)]
+PATHS = {"auto": 0, "grouped": llsa.LLSA_TEST_FORCE_GROUPED, "per_block": llsa.LLSA_TEST_FORCE_PER_BLOCK}
+
+
+def forced(path):
+    """Context manager: llsa_fwd takes `path` until exit."""
+    import contextlib
+
+    @contextlib.contextmanager
+    def ctx():
+        llsa.test_set_wait_limit(0, PATHS[path])
+        try:
+            yield
+        finally:
+            llsa.test_set_wait_limit(0, 0)
+    return ctx()
+
+
+@pytest.mark.parametrize("name,path", [(n, "auto") for n in CASES] +
+                         [(n, p) for n in GROUPABLE for p in ("grouped", "per_block")])
+def test_fwd_with_oracle_indices(case_data, name, path):
     w, x, ref = case_data(name)
-    out, _ = gpu_stage_outputs(w, x, backward=False, oracle_sel=ref["slices"])
+    with forced(path):
+        out, _ = gpu_stage_outputs(w, x, backward=False, oracle_sel=ref["slices"])
     assert_close("o", out["o"], ref["o"], w.dtype)
     assert_lse(out["lse"], ref["lse"])
 
@@ -248,7 +271,8 @@ def test_deterministic_across_runs():
         assert torch.equal(a, c)
 
 
-def test_fine_logits_far_above_pooled_logits():
+@pytest.mark.parametrize("path", ["grouped", "per_block"])
+def test_fine_logits_far_above_pooled_logits(path):
     """Keys whose block means cancel (so every pooled key is zero and every
     pooled logit is its ln B^l bias) against queries that are, on alternate
     query blocks, large multiples of the keys' direction: there the fine
@@ -273,7 +297,8 @@ def test_fine_logits_far_above_pooled_logits():
     # keeps the gradients on the scale the absolute bf16 tolerance assumes
     x["dout"] = x["dout"] / 32.0
     ref = run_oracle(w, x)
-    out, _ = gpu_stage_outputs(w, x, oracle_sel=ref["slices"])
+    with forced(path):
+        out, _ = gpu_stage_outputs(w, x, oracle_sel=ref["slices"])
     assert_close("o", out["o"], ref["o"], "bf16")
     assert_lse(out["lse"], ref["lse"])
     for key in ("dq", "dk", "dv"):

@@ -105,4 +105,6 @@ def test_pipelined_forward_times_out_then_recovers():
 
 def test_test_hook_rejects_unknown_switches():
     with pytest.raises(llsa.LLSAError):
-        llsa.test_set_wait_limit(0, 2)
+        llsa.test_set_wait_limit(0, 8)
+    with pytest.raises(llsa.LLSAError):  # both forward paths forced at once
+        llsa.test_set_wait_limit(0, llsa.LLSA_TEST_FORCE_GROUPED | llsa.LLSA_TEST_FORCE_PER_BLOCK)
