@@ -23,6 +23,10 @@
 //   warps 8-11     blocks, each with its own S and O columns in TMEM.
 // Every mbarrier wait is bounded; a timeout records LLSA_ERR_TIMEOUT and the
 // CTA drains and exits.
+//
+// Where the grouped forward (attn_fwd_grp.cu) also applies, both are launched
+// after the grouping pass and these kernels return at once when the groups
+// are large enough for it (AttnArgs::ngroups; the rule is grouped_forward).
 #include <algorithm>
 
 #include "attn.h"

@@ -150,8 +150,13 @@ int llsa_select(const llsa_params *p, const float *pyr, int32_t *sel_idx, int32_
  *   ws         : llsa_workspace_bytes(p, LLSA_OP_FWD) bytes, 16-byte aligned
  *                (0 bytes, ws may be NULL, where that is 0): the grouping of
  *                query blocks that share selected key blocks, which the
- *                tensor-core forward gathers once per group. Too small a
- *                workspace: LLSA_ERR_WORKSPACE, nothing enqueued.
+ *                grouped tensor-core forward gathers once per group. Too
+ *                small a workspace: LLSA_ERR_WORKSPACE, nothing enqueued.
+ * Where the grouped forward applies (bf16, B = 16, d = 64, K_1 in {8, 16},
+ * one enrichment column per level, L_e <= 3), the call groups the query blocks
+ * first and then takes the grouped forward when the groups hold at least 4.5
+ * query blocks on average, else the per-query-block one (decided on the
+ * device; both agree within rounding).
  * A key block listed twice in a row of sel_idx counts once (the key set is
  * the union of the listed blocks). */
 int llsa_fwd(const llsa_params *p, const void *q, const void *k, const void *v, const float *pyr,
