@@ -27,8 +27,10 @@ int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, cons
         }
         LLSA_TRY(launch_group(s, sel_idx, g, order, gdesc, ngroups, recs, st));
         // both forwards are launched; each reads the group counts and only one
-        // does the work (the other returns at once)
+        // does the work (the other returns at once); for K_1 = 4 there is no
+        // per-block tensor-core forward and the grouped one always runs
         LLSA_TRY(launch_fwd_grp(s, a, ngroups, recs, st));
+        if (!fwd_tc_supported(s)) return LLSA_OK;  // the grouped forward always runs (K_1 = 4)
         a.ngroups = ngroups;
         a.ngroups_n = s.slices * (long long)group_windows(s);
         return launch_fwd_tc(s, a, st);
@@ -48,7 +50,7 @@ int launch_bwd(const Shape& s, const void* q, const void* k, const void* v, cons
     a.sel = sel_idx; a.coarse = coarse_idx; a.col_ptr = col_ptr; a.row_idx = row_idx;
     a.dq = dq; a.dk = dk; a.dv = dv;
     carve_bwd_workspace(s, ws, &a);
-    if (fwd_tc_supported(s) && bwd_dkv_tc_fits(s)) {
+    if (bwd_tc_supported(s)) {
         LLSA_TRY(launch_bwd_dq_tc(s, a, st));
         LLSA_TRY(launch_coarse_reduce(s, a, st));
         return launch_bwd_dkv_tc(s, a, st);

@@ -109,6 +109,9 @@ int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* ngroups, co
 bool fwd_tc_supported(const Shape& s);
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
+// the tensor-core backward (dQ and dK/dV kernels): bf16, B = 16, d in {64, 128},
+// K_1 in {4, 8, 16}, one enrichment column per level
+bool bwd_tc_supported(const Shape& s);
 bool bwd_dkv_tc_fits(const Shape& s);
 int launch_bwd_dkv_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
 

@@ -1,5 +1,5 @@
 // attn_bwd_dq_tc.cu -- backward, query-major part, on the tcgen05 tensor cores
-// (bf16, B = 16, d in {64, 128}, K_1 in {8, 16}): dq, D = rowsum(dO o) (stored
+// (bf16, B = 16, d in {64, 128}, K_1 in {4, 8, 16}): dq, D = rowsum(dO o) (stored
 // with lse as (lse, D) pairs for the key-major kernel), and
 // the per-(query block, level) partial gradients of the pooled keys and values.
 //
@@ -11,7 +11,7 @@
 // scale * sum_t dS q_t and sum_t P dO_t for the pooled-level gradients.
 //
 // Per query block, key-major like the forward: S^T = K_sel Q^T and
-// dP^T = V_sel dO^T (M = 128 keys per tile, N = 16 queries), dS^T computed per
+// dP^T = V_sel dO^T (M = 128 keys per tile, 64 when K_1 = 4; N = 16 queries), dS^T computed per
 // TMEM lane and stored as the K-major operand, then dq^T = K_sel^T dS^T with
 // the same K tile read as an MN-major operand (M = d, N = 16, K = keys). The
 // softmax needs no reduction here: lse is known.
@@ -44,9 +44,11 @@ constexpr int kThreads = 384;
 constexpr int kSmemBudget = 215 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, int NT>
+template <int D, int NF_>
 struct Cfg {
-    static constexpr int NF = NT * 128;
+    static constexpr int NF = NF_;                // fine keys per query block (16 K_1)
+    static constexpr int NT = NF < 128 ? 1 : NF / 128;  // key tiles (one MMA M each)
+    static constexpr int MT = NF < 128 ? NF : 128;      // keys per tile (the MMA's M)
     static constexpr int REG = D / 64;
     static constexpr int Q_BYTES = 16 * D * 2;
     static constexpr int KV_BYTES = NF * D * 2;
@@ -72,12 +74,13 @@ struct Misc {
     int abort_flag;
 };
 
-template <int D, int NT>
+template <int D, int NF>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
                  const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mk,
                  const __grid_constant__ CUtensorMap mv, AttnArgs a) {
-    using C = Cfg<D, NT>;
+    using C = Cfg<D, NF>;
+    constexpr int NT = C::NT;
     extern __shared__ unsigned char smem_raw[];
     // 1024-byte aligned base (128-byte swizzle atoms), derived from the
     // __shared__ array by pointer arithmetic so accesses stay shared-space
@@ -91,7 +94,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long total = a.slices * (long long)a.T;
     const int G = gridDim.x;
-    const int K1 = NT * 8, Le = a.Le;
+    const int K1 = NF / 16, Le = a.Le;
     const long long mine = total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
 
     if (threadIdx.x == 0) {
@@ -198,7 +201,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             }
     } else if (warp == 1) {
         // ------------------------------------------------------- MMA issuer
-        constexpr uint32_t idS = idesc_bf16(128, 16, 0, 0);
+        constexpr uint32_t idS = idesc_bf16(C::MT, 16, 0, 0);
         constexpr uint32_t idQ = idesc_bf16(D, 16, 1, 0);
         const uint64_t dKm = desc_sw128(smem_u32(stages), 16, 1024);            // K-major
         const uint64_t dMN = desc_sw128(smem_u32(stages), C::NF * 128, 1024);   // K tile as MN-major
@@ -407,7 +410,11 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                 float s[16], dp[16];
                 tmem_ld16(tS + t * 16, s);
                 tmem_ld16(tS + 32 + t * 16, dp);
-                const int key = t * 128 + qr * 32 + lane;
+                // an M = 128 tile holds key qr * 32 + lane in this thread's TMEM
+                // lane; an M = 64 tile (K_1 = 4) holds key 16 qr + lane in lanes
+                // 0-15 of each quarter
+                const int key = C::MT == 128 ? t * 128 + qr * 32 + lane : 16 * qr + lane;
+                if (C::MT != 128 && lane >= 16) continue;
                 unsigned char* db = DS + (key >> 6) * 2048 + (key & 7) * 2;
                 const int chk = (key & 63) >> 3;
 #pragma unroll
@@ -461,17 +468,17 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
 }
 
-template <int D, int NT>
+template <int D, int NF>
 int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
-    using C = Cfg<D, NT>;
+    using C = Cfg<D, NF>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(Misc) <= 4096, "misc block");
     static_assert(C::STAGES >= 1, "one stage at least");
-    cudaFuncSetAttribute(bwd_dq_tc_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaFuncSetAttribute(bwd_dq_tc_kernel<D, NF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
     LLSA_LAUNCH("bwd_dq_tc", st,
-                bwd_dq_tc_kernel<D, NT><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a));
+                bwd_dq_tc_kernel<D, NF><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a));
     return LLSA_OK;
 }
 
@@ -482,8 +489,18 @@ int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     const long long rows = s.slices * (long long)s.n;
     const void* bases[5] = {a.q, a.dout, a.o, a.k, a.v};
     for (int t = 0; t < 5; t++) LLSA_TRY(make_tmap_bf16(&maps[t], bases[t], rows, s.d, 16));
-    if (s.d == 64) return s.K1 == 8 ? launch_cfg<64, 1>(s, a, maps, st) : launch_cfg<64, 2>(s, a, maps, st);
-    return s.K1 == 8 ? launch_cfg<128, 1>(s, a, maps, st) : launch_cfg<128, 2>(s, a, maps, st);
+    if (s.d == 64) {
+        if (s.K1 == 4) return launch_cfg<64, 64>(s, a, maps, st);
+        return s.K1 == 8 ? launch_cfg<64, 128>(s, a, maps, st) : launch_cfg<64, 256>(s, a, maps, st);
+    }
+    if (s.K1 == 4) return launch_cfg<128, 64>(s, a, maps, st);
+    return s.K1 == 8 ? launch_cfg<128, 128>(s, a, maps, st) : launch_cfg<128, 256>(s, a, maps, st);
+}
+
+bool bwd_tc_supported(const Shape& s) {
+    return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && (s.d == 64 || s.d == 128) &&
+           (s.K1 == 4 || s.K1 == 8 || s.K1 == 16) && s.Le <= 4 && s.Lc == s.Le &&
+           s.slices * (long long)s.n < (1LL << 31) && bwd_dkv_tc_fits(s);
 }
 
 }  // namespace llsa

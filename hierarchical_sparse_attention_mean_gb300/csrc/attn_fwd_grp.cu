@@ -1,6 +1,6 @@
 // attn_fwd_grp.cu -- block-sparse attention forward with KV enrichment on the
 // tcgen05 tensor cores, over groups of query blocks that share their selected
-// key blocks (bf16 in, fp32 accumulate; B = 16, d = 64, K_1 in {8, 16},
+// key blocks (bf16 in, fp32 accumulate; B = 16, d = 64, K_1 in {4, 8, 16},
 // L_e <= 3).
 //
 // Method: Pith review of arXiv 2512.16615, "Core claim": every query block of
@@ -88,6 +88,7 @@ struct GArgs {
     const int32_t* ngroups;  // groups per window of query blocks (group.cu)
     const GroupRec* recs;    // group records, at slice * T + window * win + group
     int windows, win;        // windows per slice, query blocks per window
+    int always;              // run whatever the group sizes (no per-block tensor-core forward for this shape)
 };
 
 __device__ __forceinline__ bool wait_all(uint32_t mbar, uint32_t parity, volatile int* abort_flag, int* status,
@@ -224,7 +225,7 @@ fwd_grp_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ C
     const long long total = bar->total_groups;
     // the per-query-block forward, launched after this one, takes the call
     // when the groups are too small
-    const bool run = grouped_forward(total, a.slices * (long long)T, a.test_flags);
+    const bool run = ga.always || grouped_forward(total, a.slices * (long long)T, a.test_flags);
     const long long mine = run && total > blockIdx.x ? (total - blockIdx.x + G - 1) / G : 0;
     // groups of warpgroup w: the CTA's groups w, w + 2, ...
     const long long mineW[2] = {(mine + 1) / 2, mine / 2};
@@ -676,7 +677,8 @@ int launch_k(const Shape& s, const GArgs& ga, const CUtensorMap& mq, const CUten
 }  // namespace
 
 bool fwd_grp_supported(const Shape& s) {
-    return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && s.d == 64 && (s.K1 == 8 || s.K1 == 16) && s.Le <= kLeMax &&
+    return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && s.d == 64 && (s.K1 == 4 || s.K1 == 8 || s.K1 == 16) &&
+           s.Le <= kLeMax &&
            s.Lc == s.Le && group_supported(s) && s.slices * (long long)s.n < (1LL << 31);
 }
 
@@ -693,6 +695,8 @@ int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* ngroups, co
     ga.recs = recs;
     ga.windows = group_windows(s);
     ga.win = kGroupWindow;
+    ga.always = fwd_tc_supported(s) ? 0 : 1;
+    if (s.K1 == 4) return launch_k<4>(s, ga, mq, mk, mv, st);
     return s.K1 == 8 ? launch_k<8>(s, ga, mq, mk, mv, st) : launch_k<16>(s, ga, mq, mk, mv, st);
 }
 

@@ -257,7 +257,8 @@ group_kernel(const int32_t* __restrict__ sel, int T, int K1, int bits, int windo
         if (e < nw) {
             const int i = i0 + e;
             const int32_t* row = srow + (long long)i * K1;
-            const int anc = K1 == 8 ? anchor_of<8>(row, i, T, bits)
+            const int anc = K1 == 4 ? anchor_of<4>(row, i, T, bits)
+                            : K1 == 8 ? anchor_of<8>(row, i, T, bits)
                             : K1 == 16 ? anchor_of<16>(row, i, T, bits)
                                        : anchor_generic(row, K1, i, T, bits);
             key[r] = (anc << kIdxBits) | i;
@@ -339,13 +340,14 @@ group_kernel(const int32_t* __restrict__ sel, int T, int K1, int bits, int windo
     // sorted, so the loads overlap the work.
     const int warp = tid >> 5;
     GroupRec& R = rec_s[warp];
-    if (K1 == 8) records<8>(warp, lane, ng, gst, key_s, srow, slice, T, i0, gargs, recs, status, R);
+    if (K1 == 4) records<4>(warp, lane, ng, gst, key_s, srow, slice, T, i0, gargs, recs, status, R);
+    else if (K1 == 8) records<8>(warp, lane, ng, gst, key_s, srow, slice, T, i0, gargs, recs, status, R);
     else records<16>(warp, lane, ng, gst, key_s, srow, slice, T, i0, gargs, recs, status, R);
 }
 
 }  // namespace
 
-bool group_supported(const Shape& s) { return s.T >= 1 && s.T <= (1 << kIdxBits) && (s.K1 == 8 || s.K1 == 16) && s.Le <= 4; }
+bool group_supported(const Shape& s) { return s.T >= 1 && s.T <= (1 << kIdxBits) && (s.K1 == 4 || s.K1 == 8 || s.K1 == 16) && s.Le <= 4; }
 
 size_t group_workspace_bytes(const Shape& s) {
     // order [slices][T], gdesc [slices][T], ngroups [slices][windows], records [slices][T]

@@ -85,10 +85,12 @@ def check_record(rec, members, sel_rows, coarse_rows, Le, sl):
         np.testing.assert_array_equal(ce[q, :Le], coarse_rows[m, :Le])
 
 
-@pytest.mark.parametrize("name", ["llsa-fwd-n4096-d64-b2h8-K8-bf16", "grf-64x64-K16", "n65536-grf-2heads"])
+@pytest.mark.parametrize("name", ["llsa-fwd-n4096-d64-b2h8-K8-bf16", "grf-64x64-K16", "grf-128x128-K4", "n65536-grf-2heads"])
 def test_grouping_rule_and_partition(name):
     if name == "grf-64x64-K16":
         w = synth.Workload("g", 1, 3, 4096, 64, topk=16, kind="grf", length_scale=4.0, grid=(64, 64), seed=91)
+    elif name == "grf-128x128-K4":
+        w = synth.Workload("g4", 1, 2, 16384, 64, topk=4, kind="grf", length_scale=4.0, grid=(128, 128), seed=93)
     elif name == "n65536-grf-2heads":
         w = synth.Workload("g2", 1, 2, 65536, 64, kind="grf", length_scale=8.0, grid=(256, 256), seed=92)
     else:

@@ -27,6 +27,11 @@ CASES = {
     # spatially structured field
     "d64-K16": W("d64k16", 1, 3, 4096, 64, topk=16, amplitude=0.5, seed=82),
     "d128-K8-grf": W("d128k8", 1, 3, 4096, 128, topk=8, kind="grf", length_scale=4.0, grid=(64, 64), seed=83),
+    # K_1 = 4: the grouped forward always runs (no per-block tensor-core
+    # forward for 64 keys) and the backward's dQ uses an M = 64 key tile;
+    # d = 128 takes the CUDA-core forward and the tensor-core backward
+    "d64-K4": W("d64k4", 1, 3, 4096, 64, topk=4, amplitude=0.5, seed=84),
+    "d128-K4-grf": W("d128k4", 1, 2, 4096, 128, topk=4, kind="grf", length_scale=4.0, grid=(64, 64), seed=85),
     "B4-L4-fp32": W("b4", 1, 2, 1024, 32, block=4, topk=3, dtype="fp32", seed=79),
     "B2-fig1": W("fig1", 1, 1, 8, 8, block=2, topk=1, dtype="fp32", seed=80),
     "B8-d16-bf16": W("b8", 2, 1, 512, 16, block=8, topk=5, amplitude=0.5, seed=81),
