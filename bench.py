@@ -501,6 +501,7 @@ def run_llsa(args, ws, rank, local):
     if rank == 0 and ws == 1:
         out["reorder"] = reorder_rate(w, dev, peaks)
         out["routing_recall"] = routing_recall(p, b, w, dev)
+        out["reorder_in_step"] = reorder_in_step(w, d, ms_step, dev)
     if rank == 0 and ws == 1 and not args.no_dense:
         out["dense_sdpa"] = dense_comparator(w, dev, ms_step)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -524,6 +525,69 @@ def routing_recall(p, b, w, dev):
     torch.cuda.synchronize()
     return {"value": round(llsa.routing_recall(b.sel_idx, ex), 4), "exhaustive_ms": round(e0.elapsed_time(e1), 3),
             "what": "fraction of the exhaustive level-1 Top-K held by the hierarchical selection, all query blocks"}
+
+
+def reorder_in_step(w, d, ms_tile_as_given, dev, steps: int = 50):
+    """Index reordering inside the step (token_order "raster"): pool, the
+    per-query-block forward, dQ and dK/dV read the raster tokens as 4 x 4
+    patches and write o, dq, dk, dv back in raster order. Times, on the same
+    tokens: the tile-order step on tokens permuted beforehand (the library's
+    own choice of forward, and with the per-query-block forward, whose
+    arithmetic the raster order repeats exactly), then the raster-order step,
+    and reports the routing recall of the reordered step. Events around
+    `steps` whole steps each."""
+    import hierarchical_sparse_attention_mean_gb300 as llsa
+    side = int(round(math.sqrt(w.n)))
+    pr = llsa.Params(w.batch, w.heads, w.n, w.d, block=w.block, topk=w.topk, dtype=w.dtype, token_order="raster")
+    try:
+        llsa.get_sizes(pr)
+    except llsa.LLSAError as e:
+        return {"unavailable": f"raster token order: {e}"}
+    pt = llsa.Params(w.batch, w.heads, w.n, w.d, block=w.block, topk=w.topk, dtype=w.dtype)
+    tiled = {}
+    for k, t in d.items():
+        tiled[k] = torch.empty_like(t)
+        llsa.llsa_reorder(pt, side, side, t, tiled[k])
+
+    def timed(p, x, flags=0):
+        b = llsa.Buffers(p, dev)
+        g = [torch.empty_like(x["q"]) for _ in range(3)]
+
+        def step():
+            llsa.forward(p, x["q"], x["k"], x["v"], b)
+            llsa.backward(p, x["q"], x["k"], x["v"], x["dout"], b, *g)
+
+        llsa.test_set_wait_limit(0, flags)
+        try:
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(steps):
+                step()
+            e1.record()
+            torch.cuda.synchronize()
+        finally:
+            llsa.test_set_wait_limit(0, 0)
+        if llsa.llsa_get_status() != 0:
+            raise RuntimeError("device status set in the reordered step")
+        return e0.elapsed_time(e1) / steps, b
+
+    ms_t, _ = timed(pt, tiled)
+    ms_tp, _ = timed(pt, tiled, llsa.LLSA_TEST_FORCE_PER_BLOCK)
+    ms_r, br = timed(pr, d)
+    return {"ms_per_step_raster_order": round(ms_r, 4),
+            "ms_per_step_prepermuted_per_block_forward": round(ms_tp, 4),
+            "overhead": round(ms_r / ms_tp - 1.0, 4),
+            "ms_per_step_prepermuted": round(ms_t, 4),
+            "ms_per_step_as_given": round(ms_tile_as_given, 4),
+            "routing_recall": routing_recall(pr, br, w, dev)["value"],
+            "what": f"{steps} fwd+bwd steps each on the workload's raster tokens: raster order (reordering "
+                    "inside the kernels; the per-query-block forward); the same tokens permuted beforehand, "
+                    "tile order, with the per-query-block forward (identical arithmetic: overhead) and with "
+                    "the library's choice of forward; as given = the headline step, blocks of 16 consecutive "
+                    "raster tokens (no reordering)"}
 
 
 def reorder_rate(w, dev, peaks):

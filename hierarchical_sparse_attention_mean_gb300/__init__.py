@@ -28,6 +28,8 @@ LLSA_ENRICH_TOP1 = 0
 LLSA_ENRICH_ANCESTOR = 1
 LLSA_ENRICH_ALLK = 2
 _RULES = {"top1": LLSA_ENRICH_TOP1, "ancestor": LLSA_ENRICH_ANCESTOR, "allk": LLSA_ENRICH_ALLK}
+LLSA_ORDER_TILE, LLSA_ORDER_RASTER = 0, 1
+_ORDERS = {"tile": LLSA_ORDER_TILE, "raster": LLSA_ORDER_RASTER}
 OP_POOL, OP_SELECT, OP_FWD, OP_TRANSPOSE, OP_BWD = range(5)
 MAX_LEVELS = 8
 
@@ -44,7 +46,7 @@ class _Params(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("heads", ctypes.c_int), ("n", ctypes.c_int), ("d", ctypes.c_int),
                 ("block", ctypes.c_int), ("levels", ctypes.c_int), ("topk", ctypes.c_int),
                 ("enrich_levels", ctypes.c_int), ("dtype", ctypes.c_int), ("scale", ctypes.c_float),
-                ("enrich_rule", ctypes.c_int)]
+                ("enrich_rule", ctypes.c_int), ("token_order", ctypes.c_int)]
 
 
 class _Sizes(ctypes.Structure):
@@ -116,6 +118,7 @@ class Params:
     dtype: str = "bf16"        # "bf16" or "fp32"
     scale: float = 0.0         # 0: 1/sqrt(d)
     enrich_rule: str = "top1"  # "top1", "ancestor" or "allk"
+    token_order: str = "tile"  # "tile" or "raster" (raster order of a square image)
 
     def c(self) -> _Params:
         dt = {"bf16": LLSA_DTYPE_BF16, "fp32": LLSA_DTYPE_F32}.get(self.dtype)
@@ -124,8 +127,11 @@ class Params:
         rule = _RULES.get(self.enrich_rule)
         if rule is None:
             raise ValueError(f"enrich_rule must be 'top1', 'ancestor' or 'allk', not {self.enrich_rule!r}")
+        order = _ORDERS.get(self.token_order)
+        if order is None:
+            raise ValueError(f"token_order must be 'tile' or 'raster', not {self.token_order!r}")
         return _Params(self.batch, self.heads, self.n, self.d, self.block, self.levels, self.topk,
-                       self.enrich_levels, dt, self.scale, rule)
+                       self.enrich_levels, dt, self.scale, rule, order)
 
     @staticmethod
     def like(q, **kw) -> "Params":
@@ -423,9 +429,10 @@ def _autograd_function():
         """Differentiable LLSA over [batch, heads, N, d] tensors."""
 
         @staticmethod
-        def forward(ctx, q, k, v, block, topk, levels, enrich_levels, scale):
+        def forward(ctx, q, k, v, block, topk, levels, enrich_levels, scale, token_order):
             q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
-            p = Params.like(q, block=block, topk=topk, levels=levels, enrich_levels=enrich_levels, scale=scale)
+            p = Params.like(q, block=block, topk=topk, levels=levels, enrich_levels=enrich_levels, scale=scale,
+                            token_order=token_order)
             b = forward(p, q, k, v)
             ctx.p, ctx.b = p, b
             ctx.save_for_backward(q, k, v)
@@ -435,7 +442,7 @@ def _autograd_function():
         def backward(ctx, do):
             q, k, v = ctx.saved_tensors
             dq, dk, dv = backward(ctx.p, q, k, v, do.contiguous(), ctx.b)
-            return dq, dk, dv, None, None, None, None, None
+            return dq, dk, dv, None, None, None, None, None, None
 
     return LLSAFunction
 
@@ -444,12 +451,14 @@ _FN = None
 
 
 def llsa_attention(q, k, v, block: int = 16, topk: int = 8, levels: int = 0, enrich_levels: int = -1,
-                   scale: float = 0.0):
-    """Autograd entry point: o = LLSA(q, k, v)."""
+                   scale: float = 0.0, token_order: str = "tile"):
+    """Autograd entry point: o = LLSA(q, k, v). token_order "raster": q, k, v
+    (and o, the gradients) are in the raster order of a square image, reordered
+    inside the kernels."""
     global _FN
     if _FN is None:
         _FN = _autograd_function()
-    return _FN.apply(q, k, v, block, topk, levels, enrich_levels, scale)
+    return _FN.apply(q, k, v, block, topk, levels, enrich_levels, scale, token_order)
 
 
 def default_scale(d: int) -> float:

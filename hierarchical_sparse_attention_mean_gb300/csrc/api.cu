@@ -129,6 +129,7 @@ static int derive(const llsa_params* p, Shape* s) {
         p->enrich_rule != LLSA_ENRICH_ALLK)
         return LLSA_ERR_INVALID_ARG;
     if (!(p->scale >= 0.0f) || isinf(p->scale)) return LLSA_ERR_INVALID_ARG;
+    if (p->token_order != LLSA_ORDER_TILE && p->token_order != LLSA_ORDER_RASTER) return LLSA_ERR_INVALID_ARG;
     if (p->d < 8 || p->d > 256 || p->d % 8 != 0) return LLSA_ERR_SHAPE;
     if (p->block < 2 || p->block > 1024) return LLSA_ERR_SHAPE;
     const long long n = p->n, B = p->block;
@@ -176,6 +177,14 @@ static int derive(const llsa_params* p, Shape* s) {
     if (s->Lc > kMaxCoarse) return LLSA_ERR_UNSUPPORTED;
     s->scale = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
     if (s->slices * (long long)p->n * p->d > (1LL << 40)) return LLSA_ERR_UNSUPPORTED;
+    if (p->token_order == LLSA_ORDER_RASTER) {
+        // a square image of side 4^m, blocks of 4 x 4 tokens
+        int side = 1;
+        while ((long long)side * side < p->n) side *= 4;
+        if (p->block != 16 || (long long)side * side != p->n || side < 4) return LLSA_ERR_SHAPE;
+        s->raster = 1;
+        s->side = side;
+    }
     return LLSA_OK;
 }
 

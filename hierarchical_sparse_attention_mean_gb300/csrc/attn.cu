@@ -4,7 +4,9 @@
 
 namespace llsa {
 
-size_t fwd_workspace_bytes(const Shape& s) { return fwd_grp_supported(s) ? group_workspace_bytes(s) : 0; }
+size_t fwd_workspace_bytes(const Shape& s) {
+    return fwd_grp_supported(s) && !s.raster ? group_workspace_bytes(s) : 0;
+}
 
 int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, const float* pyr,
                const int32_t* sel_idx, const int32_t* coarse_idx, void* o, float* lse, void* ws, cudaStream_t st) {
@@ -13,6 +15,8 @@ int launch_fwd(const Shape& s, const void* q, const void* k, const void* v, cons
     a.kpyr = pyr + s.slices * a.pyr_stride;
     a.vpyr = pyr + 2 * s.slices * a.pyr_stride;
     a.sel = sel_idx; a.coarse = coarse_idx; a.out_o = o; a.lse = lse;
+    // raster-order tokens: the per-query-block tensor-core forward only
+    if (s.raster) return fwd_tc_supported(s) ? launch_fwd_tc(s, a, st) : LLSA_ERR_UNSUPPORTED;
     if (fwd_grp_supported(s)) {
         int32_t *order, *gdesc, *ngroups;
         GroupRec* recs;
@@ -43,6 +47,7 @@ int launch_bwd(const Shape& s, const void* q, const void* k, const void* v, cons
                const void* dout, const float* pyr, const int32_t* sel_idx, const int32_t* coarse_idx,
                const int32_t* col_ptr, const int32_t* row_idx, void* dq, void* dk, void* dv, void* ws,
                cudaStream_t st) {
+    if (s.raster && !(bwd_tc_supported(s) && fwd_tc_supported(s))) return LLSA_ERR_UNSUPPORTED;
     AttnArgs a = make_attn_args(s);
     a.q = q; a.k = k; a.v = v; a.o = o; a.dout = dout; a.lse_in = lse;
     a.kpyr = pyr + s.slices * a.pyr_stride;

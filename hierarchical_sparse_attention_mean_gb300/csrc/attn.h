@@ -18,6 +18,7 @@ struct AttnArgs {
     float *Dbuf, *gK, *gV, *dKc, *dVc;  // backward workspace
     long long slices;
     int n, d, B, L, Le, K1, T, P;
+    int side;  // image side under LLSA_ORDER_RASTER (the kernels are instantiated per token order)
     float scale, lnB;
     LevelTable lv;
     int* status;

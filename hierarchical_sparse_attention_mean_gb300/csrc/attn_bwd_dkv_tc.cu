@@ -25,6 +25,12 @@
 // each softmax thread loads its query row's (lse, D) pair itself, one item
 // ahead; warp 1 issues the S stream and warp 12 the gradient stream, each in
 // order with blocking waits, through an election inside the MMA asm.
+//
+// Token order: each kernel is built for the tile order and for the raster order
+// of a square image (index reordering, referee comments on Sec. 5.1 and
+// Figure 2): in the latter a block's tokens come in as one 4 x 4 patch (a 4-D
+// TMA box landing in the same swizzled layout) and its output rows go back to
+// the patch's pixels; the arithmetic is the same.
 #include <algorithm>
 
 #include "attn.h"
@@ -91,7 +97,7 @@ struct ItemWalk {
     }
 };
 
-template <int D>
+template <int D, bool R>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
                   const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv, AttnArgs a) {
@@ -232,15 +238,24 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 if (lane == 0) {
                     const int yk = (int)(slice * a.n + (long long)j * 16);
                     for (int r = 0; r < C::REG; r++) {
-                        tma_load_2d(smem_u32(sb + C::OFF_K + r * 2048), &mk, r * 64, yk, fb);
-                        tma_load_2d(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, yk, fb);
+                        if constexpr (R) {
+                            tma_load_block<true>(smem_u32(sb + C::OFF_K + r * 2048), &mk, r * 64, slice, j, a.n, fb);
+                            tma_load_block<true>(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, slice, j, a.n, fb);
+                        } else {
+                            tma_load_2d(smem_u32(sb + C::OFF_K + r * 2048), &mk, r * 64, yk, fb);
+                            tma_load_2d(smem_u32(sb + C::OFF_V + r * 2048), &mv, r * 64, yk, fb);
+                        }
                     }
                 }
             } else if (lane < nv) {
                 const int off = role == 1 ? 0 : C::OFF_DO;
                 const CUtensorMap* map = role == 1 ? &mq : &mdo;
-                for (int r = 0; r < C::REG; r++)
-                    tma_load_2d(smem_u32(sb + off + r * 128 * 128 + lane * 2048), map, r * 64, (int)tok, fb);
+                for (int r = 0; r < C::REG; r++) {
+                    if constexpr (R)
+                        tma_load_block<true>(smem_u32(sb + off + r * 128 * 128 + lane * 2048), map, r * 64, slice, qb, a.n, fb);
+                    else
+                        tma_load_2d(smem_u32(sb + off + r * 128 * 128 + lane * 2048), map, r * 64, (int)tok, fb);
+                }
             }
             issued = n;
         }
@@ -380,16 +395,24 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 fv = fmaf(prv[l], inv, fv);
                 span *= a.B;
             }
-            const long long row0 = (pslice * a.n + (long long)pj * 16) * D + dd;
+            // the block's rows, contiguous in tile order, a 4 x 4 patch in raster order
+            long long row0 = (pslice * a.n + (long long)pj * 16) * D + dd;
+            if constexpr (R) row0 = token_row(pslice, a.n, 1, a.side, pj * 16) * D + dd;
             if (is_k) {
                 __nv_bfloat16* dk = static_cast<__nv_bfloat16*>(a.dk) + row0;
 #pragma unroll
-                for (int c = 0; c < 16; c++) dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+                for (int c = 0; c < 16; c++) {
+                    if constexpr (R) dk[block_token_offset(c, a.side) * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+                    else dk[c * D] = __float2bfloat16_rn(fmaf(sc, kk[c], fk));
+                }
             }
             if (D == 128 || !is_k) {
                 __nv_bfloat16* dv = static_cast<__nv_bfloat16*>(a.dv) + row0;
 #pragma unroll
-                for (int c = 0; c < 16; c++) dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
+                for (int c = 0; c < 16; c++) {
+                    if constexpr (R) dv[block_token_offset(c, a.side) * D] = __float2bfloat16_rn(vv[c] + fv);
+                    else dv[c * D] = __float2bfloat16_rn(vv[c] + fv);
+                }
             }
         };
         // (lse, D) of this thread's query row for one of the group's items,
@@ -509,19 +532,25 @@ bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     }
 }
 
-template <int D>
-int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
+template <int D, bool R>
+int launch_one(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
     using C = Cfg<D>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(Misc) <= 4096, "misc block");
     static_assert(C::STAGES >= 1, "one stage at least");
-    cudaFuncSetAttribute(bwd_dkv_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaFuncSetAttribute(bwd_dkv_tc_kernel<D, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
     if ((total + grid - 1) / grid > kMaxKeyBlocks) return LLSA_ERR_UNSUPPORTED;
     LLSA_LAUNCH("bwd_dkv_tc", st,
-                bwd_dkv_tc_kernel<D><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], a));
+                bwd_dkv_tc_kernel<D, R><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], a));
     return LLSA_OK;
+}
+
+// each built once per token order
+template <int D>
+int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
+    return s.raster ? launch_one<D, true>(s, a, maps, st) : launch_one<D, false>(s, a, maps, st);
 }
 
 }  // namespace
@@ -534,9 +563,8 @@ bool bwd_dkv_tc_fits(const Shape& s) {
 
 int launch_bwd_dkv_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     CUtensorMap maps[4];
-    const long long rows = s.slices * (long long)s.n;
     const void* bases[4] = {a.q, a.dout, a.k, a.v};
-    for (int t = 0; t < 4; t++) LLSA_TRY(make_tmap_bf16(&maps[t], bases[t], rows, s.d, 16));
+    for (int t = 0; t < 4; t++) LLSA_TRY(make_tmap_tokens(&maps[t], bases[t], s));
     return s.d == 64 ? launch_cfg<64>(s, a, maps, st) : launch_cfg<128>(s, a, maps, st);
 }
 

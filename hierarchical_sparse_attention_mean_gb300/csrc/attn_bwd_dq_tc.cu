@@ -30,6 +30,12 @@
 // the S stream and the gradient stream (gradient first, as it frees a stage),
 // through an election inside the MMA asm; two warpgroups alternate query
 // blocks.
+//
+// Token order: each kernel is built for the tile order and for the raster order
+// of a square image (index reordering, referee comments on Sec. 5.1 and
+// Figure 2): in the latter a block's tokens come in as one 4 x 4 patch (a 4-D
+// TMA box landing in the same swizzled layout) and its output rows go back to
+// the patch's pixels; the arithmetic is the same.
 #include <algorithm>
 
 #include "attn.h"
@@ -74,7 +80,7 @@ struct Misc {
     int abort_flag;
 };
 
-template <int D, int NF>
+template <int D, int NF, bool R>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mdo,
                  const __grid_constant__ CUtensorMap mo, const __grid_constant__ CUtensorMap mk,
@@ -164,9 +170,15 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             if (role == 0) {
                 if (lane == 0) {
                     for (int r = 0; r < C::REG; r++) {
-                        tma_load_2d(smem_u32(sb + r * 2048), &mq, r * 64, (int)tok0, fb);
-                        tma_load_2d(smem_u32(sb + C::OFF_DO + r * 2048), &mdo, r * 64, (int)tok0, fb);
-                        tma_load_2d(smem_u32(sb + C::OFF_O + r * 2048), &mo, r * 64, (int)tok0, fb);
+                        if constexpr (R) {
+                            tma_load_block<true>(smem_u32(sb + r * 2048), &mq, r * 64, slice, i, a.n, fb);
+                            tma_load_block<true>(smem_u32(sb + C::OFF_DO + r * 2048), &mdo, r * 64, slice, i, a.n, fb);
+                            tma_load_block<true>(smem_u32(sb + C::OFF_O + r * 2048), &mo, r * 64, slice, i, a.n, fb);
+                        } else {
+                            tma_load_2d(smem_u32(sb + r * 2048), &mq, r * 64, (int)tok0, fb);
+                            tma_load_2d(smem_u32(sb + C::OFF_DO + r * 2048), &mdo, r * 64, (int)tok0, fb);
+                            tma_load_2d(smem_u32(sb + C::OFF_O + r * 2048), &mo, r * 64, (int)tok0, fb);
+                        }
                     }
                     bulk_load(smem_u32(sb + C::OFF_L), a.lse_in + tok0, 64, fb);
                 }
@@ -184,10 +196,19 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                     set_status(a.status, LLSA_ERR_BAD_INDEX);
                     ix = 0;
                 }
-                const int yk = (int)(slice * a.n + (long long)ix * 16);
+                const int yk = R ? ix : (int)(slice * a.n + (long long)ix * 16);
                 for (int r = 0; r < C::REG; r++) {
-                    if (role == 1) tma_load_2d(smem_u32(sb + C::OFF_K + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
-                    else tma_load_2d(smem_u32(sb + C::OFF_V + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    if constexpr (R) {
+                        if (role == 1)
+                            tma_load_block<true>(smem_u32(sb + C::OFF_K + r * C::NF * 128 + lane * 2048), &mk, r * 64,
+                                                 slice, yk, a.n, fb);
+                        else
+                            tma_load_block<true>(smem_u32(sb + C::OFF_V + r * C::NF * 128 + lane * 2048), &mv, r * 64,
+                                                 slice, yk, a.n, fb);
+                    } else {
+                        if (role == 1) tma_load_2d(smem_u32(sb + C::OFF_K + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
+                        else tma_load_2d(smem_u32(sb + C::OFF_V + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    }
                 }
             }
             issued = bl;
@@ -439,7 +460,12 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             tc_fence_before();
             mbar_arrive(smem_u32(&ms->o_free[w]));
             if (valid) {
+                // the block's rows: tok0 .. +15 in tile order, a 4 x 4 patch in raster order
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq) + tok0 * D + dd;
+                if constexpr (R) {
+                    const long long sl = g / a.T;
+                    dst = static_cast<__nv_bfloat16*>(a.dq) + token_row(sl, a.n, 1, a.side, (int)(tok0 - sl * a.n)) * D + dd;
+                }
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
                     const float4 g4 = *reinterpret_cast<const float4*>(ms->cds[w][j & 1][c]);
@@ -448,7 +474,8 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                     val = fmaf(g4.y, kc[1], val);
                     val = fmaf(g4.z, kc[2], val);
                     val = fmaf(g4.w, kc[3], val);
-                    dst[c * D] = __float2bfloat16_rn(sc * val);
+                    if constexpr (R) dst[block_token_offset(c, a.side) * D] = __float2bfloat16_rn(sc * val);
+                    else dst[c * D] = __float2bfloat16_rn(sc * val);
                 }
                 const long long off = g * (long long)a.Le * D + dd;
 #pragma unroll
@@ -468,27 +495,32 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     }
 }
 
-template <int D, int NF>
-int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
+template <int D, int NF, bool R>
+int launch_one(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
     using C = Cfg<D, NF>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(Misc) <= 4096, "misc block");
     static_assert(C::STAGES >= 1, "one stage at least");
-    cudaFuncSetAttribute(bwd_dq_tc_kernel<D, NF>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaFuncSetAttribute(bwd_dq_tc_kernel<D, NF, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
     LLSA_LAUNCH("bwd_dq_tc", st,
-                bwd_dq_tc_kernel<D, NF><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a));
+                bwd_dq_tc_kernel<D, NF, R><<<grid, kThreads, C::SMEM, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a));
     return LLSA_OK;
+}
+
+// each built once per token order
+template <int D, int NF>
+int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap* maps, cudaStream_t st) {
+    return s.raster ? launch_one<D, NF, true>(s, a, maps, st) : launch_one<D, NF, false>(s, a, maps, st);
 }
 
 }  // namespace
 
 int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     CUtensorMap maps[5];
-    const long long rows = s.slices * (long long)s.n;
     const void* bases[5] = {a.q, a.dout, a.o, a.k, a.v};
-    for (int t = 0; t < 5; t++) LLSA_TRY(make_tmap_bf16(&maps[t], bases[t], rows, s.d, 16));
+    for (int t = 0; t < 5; t++) LLSA_TRY(make_tmap_tokens(&maps[t], bases[t], s));
     if (s.d == 64) {
         if (s.K1 == 4) return launch_cfg<64, 64>(s, a, maps, st);
         return s.K1 == 8 ? launch_cfg<64, 128>(s, a, maps, st) : launch_cfg<64, 256>(s, a, maps, st);

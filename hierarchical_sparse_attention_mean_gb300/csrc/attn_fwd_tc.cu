@@ -27,6 +27,12 @@
 // Where the grouped forward (attn_fwd_grp.cu) also applies, both are launched
 // after the grouping pass and these kernels return at once when the groups
 // are large enough for it (AttnArgs::ngroups; the rule is grouped_forward).
+//
+// Token order: each kernel is built for the tile order and for the raster order
+// of a square image (index reordering, referee comments on Sec. 5.1 and
+// Figure 2): in the latter a block's tokens come in as one 4 x 4 patch (a 4-D
+// TMA box landing in the same swizzled layout) and its output rows go back to
+// the patch's pixels; the arithmetic is the same.
 #include <algorithm>
 
 #include "attn.h"
@@ -83,7 +89,7 @@ struct Misc {
     int abort_flag;
 };
 
-template <int D, int NT>
+template <int D, int NT, bool R>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, AttnArgs a) {
@@ -183,17 +189,25 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) {
                 const int yq = (int)(slice * a.n + (long long)i * 16);
-                for (int r = 0; r < C::REG; r++) tma_load_2d(smem_u32(sQ + r * 16 * 128), &mq, r * 64, yq, fb);
+                for (int r = 0; r < C::REG; r++) {
+                    if constexpr (R) tma_load_block<true>(smem_u32(sQ + r * 16 * 128), &mq, r * 64, slice, i, a.n, fb);
+                    else tma_load_2d(smem_u32(sQ + r * 16 * 128), &mq, r * 64, yq, fb);
+                }
             }
             if (lane < K1) {
                 if (jb < 0 || jb >= a.T) {
                     set_status(a.status, LLSA_ERR_BAD_INDEX);
                     jb = 0;
                 }
-                const int yk = (int)(slice * a.n + (long long)jb * 16);
+                const int yk = R ? jb : (int)(slice * a.n + (long long)jb * 16);
                 for (int r = 0; r < C::REG; r++) {
-                    tma_load_2d(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
-                    tma_load_2d(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    if constexpr (R) {
+                        tma_load_block<true>(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, slice, yk, a.n, fb);
+                        tma_load_block<true>(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, slice, yk, a.n, fb);
+                    } else {
+                        tma_load_2d(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
+                        tma_load_2d(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    }
                 }
             }
             if (lane < Le) {
@@ -428,7 +442,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tc_fence_before();
             mbar_arrive(smem_u32(&ms->o_free[w]));
             if (valid) {
+                // the block's rows, contiguous in tile order, a 4 x 4 patch in raster order
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out_o) + (slice * a.n + (long long)i * 16) * D + dd;
+                if constexpr (R) dst = static_cast<__nv_bfloat16*>(a.out_o) + token_row(slice, a.n, 1, a.side, i * 16) * D + dd;
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
                     const float4 pz = *reinterpret_cast<const float4*>(ms->ecs[w][c]);
@@ -437,7 +453,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     val = fmaf(pz.y, vc[1], val);
                     val = fmaf(pz.z, vc[2], val);
                     val = fmaf(pz.w, vc[3], val);
-                    dst[c * D] = __float2bfloat16_rn(val);
+                    if constexpr (R) dst[block_token_offset(c, a.side) * D] = __float2bfloat16_rn(val);
+                    else dst[c * D] = __float2bfloat16_rn(val);
                 }
             }
         }
@@ -512,7 +529,7 @@ struct PMisc {
     int abort_flag;
 };
 
-template <int D, int NT>
+template <int D, int NT, bool R>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, AttnArgs a) {
@@ -604,17 +621,27 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             __syncwarp();
             if (role == 0 && lane == 0) {
                 const int yq = (int)(slice * a.n + (long long)i * 16);
-                for (int r = 0; r < C::REG; r++) tma_load_2d(smem_u32(sQ + r * 16 * 128), &mq, r * 64, yq, fb);
+                for (int r = 0; r < C::REG; r++) {
+                    if constexpr (R) tma_load_block<true>(smem_u32(sQ + r * 16 * 128), &mq, r * 64, slice, i, a.n, fb);
+                    else tma_load_2d(smem_u32(sQ + r * 16 * 128), &mq, r * 64, yq, fb);
+                }
             }
             if (role < 2 && lane < K1) {
                 if (ix < 0 || ix >= a.T) {
                     set_status(a.status, LLSA_ERR_BAD_INDEX);
                     ix = 0;
                 }
-                const int yk = (int)(slice * a.n + (long long)ix * 16);
+                const int yk = R ? ix : (int)(slice * a.n + (long long)ix * 16);
                 for (int r = 0; r < C::REG; r++) {
-                    if (role == 0) tma_load_2d(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
-                    else tma_load_2d(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    if constexpr (R) {
+                        if (role == 0)
+                            tma_load_block<true>(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, slice, yk, a.n, fb);
+                        else
+                            tma_load_block<true>(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, slice, yk, a.n, fb);
+                    } else {
+                        if (role == 0) tma_load_2d(smem_u32(sK + r * C::NF * 128 + lane * 2048), &mk, r * 64, yk, fb);
+                        else tma_load_2d(smem_u32(sV + r * C::NF * 128 + lane * 2048), &mv, r * 64, yk, fb);
+                    }
                 }
             }
             if (role == 2 && lane < Le) {
@@ -799,7 +826,9 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             tc_fence_before();
             mbar_arrive(smem_u32(&ms->o_free[w][b]));
             if (valid) {
+                // the block's rows, contiguous in tile order, a 4 x 4 patch in raster order
                 __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out_o) + (slice * a.n + (long long)i * 16) * D + dd;
+                if constexpr (R) dst = static_cast<__nv_bfloat16*>(a.out_o) + token_row(slice, a.n, 1, a.side, i * 16) * D + dd;
 #pragma unroll
                 for (int c = 0; c < 16; c++) {
                     const float4 pz = *reinterpret_cast<const float4*>(ms->ecs[w][b][c]);
@@ -808,7 +837,8 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                     val = fmaf(pz.y, vcp[1], val);
                     val = fmaf(pz.z, vcp[2], val);
                     val = fmaf(pz.w, vcp[3], val);
-                    dst[c * D] = __float2bfloat16_rn(val);
+                    if constexpr (R) dst[block_token_offset(c, a.side) * D] = __float2bfloat16_rn(val);
+                    else dst[c * D] = __float2bfloat16_rn(val);
                 }
             }
         };
@@ -948,38 +978,42 @@ fwd_tc_pipe_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     }
 }
 
-template <int D, int NT>
+template <int D, int NT, bool R>
 int launch_pipe(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                 const CUtensorMap& mv, cudaStream_t st) {
     using C = PCfg<D, NT>;
     static_assert(C::SMEM <= 227 * 1024 && C::STAGES >= 4, "shared memory budget");
     static_assert(sizeof(PMisc) <= 8192, "misc block");
-    cudaFuncSetAttribute(fwd_tc_pipe_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaFuncSetAttribute(fwd_tc_pipe_kernel<D, NT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
-    LLSA_LAUNCH("fwd_tc", st, fwd_tc_pipe_kernel<D, NT><<<grid, kThreads, C::SMEM, st>>>(mq, mk, mv, a));
+    LLSA_LAUNCH("fwd_tc", st, fwd_tc_pipe_kernel<D, NT, R><<<grid, kThreads, C::SMEM, st>>>(mq, mk, mv, a));
     return LLSA_OK;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool R>
 int launch_cfg(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                const CUtensorMap& mv, cudaStream_t st) {
     using C = Cfg<D, NT>;
     static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
     static_assert(sizeof(Misc) <= 4096, "misc block");
-    cudaFuncSetAttribute(fwd_tc_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaFuncSetAttribute(fwd_tc_kernel<D, NT, R>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     const long long total = s.slices * (long long)s.T;
     const int grid = (int)std::min<long long>(total, (long long)sm_count());
-    LLSA_LAUNCH("fwd_tc", st, fwd_tc_kernel<D, NT><<<grid, kThreads, C::SMEM, st>>>(mq, mk, mv, a));
+    LLSA_LAUNCH("fwd_tc", st, fwd_tc_kernel<D, NT, R><<<grid, kThreads, C::SMEM, st>>>(mq, mk, mv, a));
     return LLSA_OK;
 }
 
-// the pipelined kernel where four stages fit, else the few-stage one
+// the pipelined kernel where four stages fit, else the few-stage one; each
+// built once per token order
 template <int D, int NT>
 int launch_any(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const CUtensorMap& mk,
                const CUtensorMap& mv, cudaStream_t st) {
-    if constexpr (pipe_fits<D, NT>()) return launch_pipe<D, NT>(s, a, mq, mk, mv, st);
-    else return launch_cfg<D, NT>(s, a, mq, mk, mv, st);
+    if constexpr (pipe_fits<D, NT>()) {
+        return s.raster ? launch_pipe<D, NT, true>(s, a, mq, mk, mv, st) : launch_pipe<D, NT, false>(s, a, mq, mk, mv, st);
+    } else {
+        return s.raster ? launch_cfg<D, NT, true>(s, a, mq, mk, mv, st) : launch_cfg<D, NT, false>(s, a, mq, mk, mv, st);
+    }
 }
 
 }  // namespace
@@ -992,10 +1026,9 @@ bool fwd_tc_supported(const Shape& s) {
 
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     CUtensorMap mq, mk, mv;
-    const long long rows = s.slices * (long long)s.n;
-    LLSA_TRY(make_tmap_bf16(&mq, a.q, rows, s.d, 16));
-    LLSA_TRY(make_tmap_bf16(&mk, a.k, rows, s.d, 16));
-    LLSA_TRY(make_tmap_bf16(&mv, a.v, rows, s.d, 16));
+    LLSA_TRY(make_tmap_tokens(&mq, a.q, s));
+    LLSA_TRY(make_tmap_tokens(&mk, a.k, s));
+    LLSA_TRY(make_tmap_tokens(&mv, a.v, s));
     if (s.d == 64) return s.K1 == 8 ? launch_any<64, 1>(s, a, mq, mk, mv, st) : launch_any<64, 2>(s, a, mq, mk, mv, st);
     return s.K1 == 8 ? launch_any<128, 1>(s, a, mq, mk, mv, st) : launch_any<128, 2>(s, a, mq, mk, mv, st);
 }

@@ -601,6 +601,7 @@ AttnArgs make_attn_args(const Shape& s) {
     a.pyr_stride = (long long)s.P * s.d;
     a.slices = s.slices;
     a.n = s.n; a.d = s.d; a.B = s.B; a.L = s.L; a.Le = s.Le; a.K1 = s.K1; a.T = s.T; a.P = s.P;
+    a.side = s.side;
     a.scale = s.scale;
     a.lnB = logf((float)s.B);
     a.lv = level_table(s);

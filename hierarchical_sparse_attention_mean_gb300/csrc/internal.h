@@ -20,6 +20,7 @@ struct Shape {
     float scale;
     int rule;  // enrichment rule (LLSA_ENRICH_*)
     int topk;  // K as requested (before the per-level clamp)
+    int raster, side;  // token tensors in the raster order of a side x side image (LLSA_ORDER_RASTER)
     // enrichment columns: C per coarse_idx row (levels 1..L), Lc of them used
     // (levels 1..L_e, a prefix); level l owns columns col_off[l] .. col_off[l+1]-1
     int C, Lc;
@@ -46,6 +47,39 @@ inline LevelTable level_table(const Shape& s) {
         t.n_level[l] = s.n_level[l];
     }
     return t;
+}
+
+// ----------------------------------------------------------- token order --
+
+// The kernels work in the hierarchical tile order. With B = 16 the blocks of
+// 16 consecutive tokens are 4 x 4 patches of the image: block b's base-16
+// digits (finest first) are row digit * 4 + column digit of its patch, so the
+// patch's top-left pixel is (4 py, 4 px), and token w of the block is pixel
+// (4 py + w / 4, 4 px + w % 4). Under LLSA_ORDER_RASTER the token tensors are
+// addressed through these two maps instead of being permuted first.
+__host__ __device__ __forceinline__ void block_patch(int b, int& px, int& py) {
+    px = 0;
+    py = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        px |= ((b >> (4 * k)) & 3) << (2 * k);
+        py |= ((b >> (4 * k + 2)) & 3) << (2 * k);
+    }
+}
+
+// Row (in [slices * n]) of the token at tile position t of slice `slice`.
+__host__ __device__ __forceinline__ long long token_row(long long slice, int n, int raster, int side, int t) {
+    if (!raster) return slice * n + t;
+    int px, py;
+    block_patch(t >> 4, px, py);
+    return slice * n + (long long)(4 * py + ((t >> 2) & 3)) * side + 4 * px + (t & 3);
+}
+
+// Rows from a block's first token to its token w: w in tile order
+// (row_stride 4), or row w / 4 and column w % 4 of the block's patch in raster
+// order (row_stride = the image side).
+__host__ __device__ __forceinline__ long long block_token_offset(int w, int row_stride) {
+    return (long long)(w >> 2) * row_stride + (w & 3);
 }
 
 // ------------------------------------------------------------ launching --

@@ -9,7 +9,10 @@
 // a chunk of up to 4096 consecutive tokens of one tensor of one slice, writes
 // its level-1 rows, then derives the coarser levels of the chunk from the rows
 // it just wrote (L1/L2-resident). Levels whose blocks are longer than a chunk
-// (only when B^L > 4096) are finished by a second small kernel.
+// (only when B^L > 4096) are finished by a second small kernel. Under
+// LLSA_ORDER_RASTER (index reordering, referee comments on Sec. 5.1 and
+// Figure 2) the inputs are read in place as 4 x 4 token patches, so the
+// pyramid is the one of the reordered tokens without a reordering pass.
 #include "internal.h"
 
 namespace llsa {
@@ -23,6 +26,7 @@ struct PoolArgs {
     float* pyr;
     long long slices;
     int n, d, B, P;
+    int raster, side;  // inputs in the raster order of a side x side image (B = 16)
     int chunk, levels_in_chunk;
     LevelTable lv;
 };
@@ -46,7 +50,7 @@ __device__ __forceinline__ float4 mean_rows(const float* prev, long long r, int 
     return make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
 }
 
-template <typename T>
+template <typename T, bool R>
 __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
     const int tensor = blockIdx.y;
     const int nchunks = a.n / a.chunk;
@@ -58,7 +62,10 @@ __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
     const float inv = 1.0f / (float)B;
 
     // level 1: each item sums B input rows over 8 channels (one 16-byte vector
-    // for bf16); consecutive threads take consecutive vectors of a row.
+    // for bf16); consecutive threads take consecutive vectors of a row. Level-1
+    // row r of the chunk is block b = c * rows + r of the slice: tokens 16 b ..
+    // in tile order, or the block's 4 x 4 patch of the raster image, summed in
+    // the same (tile) order.
     {
         const int rows = a.chunk / B;
         const int V = d / 8;
@@ -66,6 +73,8 @@ __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
         for (int item = threadIdx.x; item < rows * V; item += kPoolThreads) {
             const int r = item / V, vv = item % V;
             const T* src = x + (long long)r * B * d + vv * 8;
+            if constexpr (R)  // block c * rows + r of the slice, from the tensor's base
+                src = static_cast<const T*>(a.x[tensor]) + token_row(slice, a.n, 1, a.side, (c * rows + r) * B) * d + vv * 8;
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) acc[i] = 0.f;
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
             for (; cc + 8 <= B; cc += 8) {
                 float f[8][8];
 #pragma unroll
-                for (int u = 0; u < 8; u++) load8(src + (long long)(cc + u) * d, f[u]);
+                for (int u = 0; u < 8; u++) load8(src + (R ? block_token_offset(cc + u, a.side) : (long long)(cc + u)) * d, f[u]);
 #pragma unroll
                 for (int u = 0; u < 8; u++)
 #pragma unroll
@@ -81,7 +90,7 @@ __global__ void __launch_bounds__(kPoolThreads) pool_chunk_kernel(PoolArgs a) {
             }
             for (; cc < B; cc++) {
                 float f[8];
-                load8(src + (long long)cc * d, f);
+                load8(src + (R ? block_token_offset(cc, a.side) : (long long)cc) * d, f);
 #pragma unroll
                 for (int i = 0; i < 8; i++) acc[i] += f[i];
             }
@@ -132,6 +141,7 @@ int launch_pool(const Shape& s, const void* q, const void* k, const void* v, flo
     PoolArgs a;
     a.x[0] = q; a.x[1] = k; a.x[2] = v;
     a.pyr = pyr; a.slices = s.slices; a.n = s.n; a.d = s.d; a.B = s.B; a.P = s.P;
+    a.raster = s.raster; a.side = s.side;
     a.lv = level_table(s);
     // largest level whose blocks fit in one chunk, then widen the chunk by
     // powers of two while it still divides N
@@ -146,10 +156,15 @@ int launch_pool(const Shape& s, const void* q, const void* k, const void* v, flo
     const long long blocks = s.slices * (s.n / chunk);
     if (blocks > 0x7fffffffLL) return LLSA_ERR_UNSUPPORTED;
     dim3 grid((unsigned)blocks, 3);
-    if (s.dtype == LLSA_DTYPE_BF16)
-        LLSA_LAUNCH("pool_chunk", st, pool_chunk_kernel<__nv_bfloat16><<<grid, kPoolThreads, 0, st>>>(a));
+    // one instance per dtype and token order
+    if (s.dtype == LLSA_DTYPE_BF16 && s.raster)
+        LLSA_LAUNCH("pool_chunk", st, pool_chunk_kernel<__nv_bfloat16, true><<<grid, kPoolThreads, 0, st>>>(a));
+    else if (s.dtype == LLSA_DTYPE_BF16)
+        LLSA_LAUNCH("pool_chunk", st, pool_chunk_kernel<__nv_bfloat16, false><<<grid, kPoolThreads, 0, st>>>(a));
+    else if (s.raster)
+        LLSA_LAUNCH("pool_chunk", st, pool_chunk_kernel<float, true><<<grid, kPoolThreads, 0, st>>>(a));
     else
-        LLSA_LAUNCH("pool_chunk", st, pool_chunk_kernel<float><<<grid, kPoolThreads, 0, st>>>(a));
+        LLSA_LAUNCH("pool_chunk", st, pool_chunk_kernel<float, false><<<grid, kPoolThreads, 0, st>>>(a));
     if (lc < s.L)
         LLSA_LAUNCH("pool_upper", st,
                     pool_upper_kernel<<<dim3((unsigned)s.slices, 3), kPoolThreads, 0, st>>>(a, lc + 1, s.L));

@@ -147,6 +147,32 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
                  :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(mbar) : "memory");
 }
 
+// 4D tiled TMA load (box from the tensor map), completing bytes on the mbarrier.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint32_t mbar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(mbar) : "memory");
+}
+
+// Block b (16 tokens) of slice `slice` of a token tensor, columns col ..
+// col + 63, through a map from make_tmap_tokens: rows slice * n + 16 b ..
+// +15 in tile order, or (RASTER) the block's 4 x 4 patch of the raster image.
+// Both land as 16 rows of 128 bytes in the same swizzled layout. The order is
+// a compile-time choice: each kernel is built once per order, so the tile
+// order's copies carry no raster code.
+template <bool RASTER>
+__device__ __forceinline__ void tma_load_block(uint32_t dst, const CUtensorMap* map, int col, long long slice, int b,
+                                               int n, uint32_t mbar) {
+    if constexpr (RASTER) {
+        int px, py;
+        block_patch(b, px, py);
+        tma_load_4d(dst, map, col, 4 * px, 4 * py, (int)slice, mbar);
+    } else {
+        tma_load_2d(dst, map, col, (int)(slice * n + (long long)b * 16), mbar);
+    }
+}
+
 // 1D bulk copy global -> shared (16-byte aligned addresses, size a multiple
 // of 16), completing bytes on the mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t mbar) {
@@ -302,5 +328,11 @@ __device__ __forceinline__ float warp_reduce16(const float* v, int lane) {
 // of 16 rows x 64 columns and 128-byte swizzle (the layout the descriptors
 // above describe). Returns LLSA_OK or LLSA_ERR_CUDA.
 int make_tmap_bf16(CUtensorMap* map, const void* base, long long rows, int cols, int box_rows);
+
+// Host: the tensor map of a bf16 token tensor [slices][n][d] for
+// tma_load_block: the 2D map above (16-row boxes) in tile order, or under
+// LLSA_ORDER_RASTER a 4D map [slices][side][side][d] with 4 x 4 token boxes
+// of 64 columns and the same swizzle.
+int make_tmap_tokens(CUtensorMap* map, const void* base, const Shape& s);
 
 }  // namespace llsa

@@ -67,6 +67,21 @@ enum { LLSA_DTYPE_BF16 = 0, LLSA_DTYPE_F32 = 1 };
  *       level instead of one, each with weight B^l). */
 enum { LLSA_ENRICH_TOP1 = 0, LLSA_ENRICH_ANCESTOR = 1, LLSA_ENRICH_ALLK = 2 };
 
+/* Token order of q, k, v, o, dout, dq, dk and dv (referee comments on Sec. 5.1
+ * and Figure 2, index reordering; the ordering is the one llsa_reorder
+ * computes). LLSA_ORDER_TILE: the tokens are already in the hierarchical tile
+ * order, so every block of B consecutive tokens is compact in the image.
+ * LLSA_ORDER_RASTER: they are in the raster order of a square image of side
+ * sqrt(N); pool, forward and backward read and write them in place of a
+ * reordering pass, working in tile order inside. Needs B = 16 and a side of
+ * 4^m (LLSA_ERR_SHAPE otherwise); llsa_fwd and llsa_bwd take it only on the
+ * per-query-block tensor-core kernels (bf16, d in {64, 128}, K_1 in {8, 16},
+ * one coarse token per level; the forward needs no workspace then), else
+ * LLSA_ERR_UNSUPPORTED. Everything that is not a token
+ * tensor keeps the tile order: pyr, lse, sel_idx, coarse_idx, level_idx,
+ * col_ptr and row_idx index blocks and tokens by tile position. */
+enum { LLSA_ORDER_TILE = 0, LLSA_ORDER_RASTER = 1 };
+
 enum { LLSA_OP_POOL = 0, LLSA_OP_SELECT = 1, LLSA_OP_FWD = 2, LLSA_OP_TRANSPOSE = 3, LLSA_OP_BWD = 4 };
 
 typedef struct llsa_params {
@@ -80,6 +95,7 @@ typedef struct llsa_params {
     int dtype;          /* LLSA_DTYPE_BF16 or LLSA_DTYPE_F32 */
     float scale;        /* softmax scale; 0 selects 1/sqrt(d) */
     int enrich_rule;    /* LLSA_ENRICH_TOP1, LLSA_ENRICH_ANCESTOR or LLSA_ENRICH_ALLK */
+    int token_order;    /* LLSA_ORDER_TILE (0) or LLSA_ORDER_RASTER */
 } llsa_params;
 
 /* Sizes derived from the parameters. */

@@ -142,3 +142,24 @@ def test_test_hook_flags(lib):
     for f in (llsa.LLSA_TEST_FORCE_GROUPED, llsa.LLSA_TEST_FORCE_PER_BLOCK, llsa.LLSA_TEST_NO_COPIES, 0):
         assert lib.llsa_test_set_wait_limit(0, f) == 0
     assert lib.llsa_test_set_wait_limit(0, 0) == 0
+
+
+def test_token_order_validation(lib):
+    # raster order: B = 16 and a square image of side 4^m
+    for n in (256, 4096, 65536, 1 << 20):
+        s = llsa.get_sizes(llsa.Params(1, 2, n, 64, token_order="raster"))
+        assert s.n_blocks == n // 16
+    for kw, code in ((dict(n=1024), -2),                     # side 32 is not a power of 4
+                     (dict(n=512 * 512), -2),                # nor is 512
+                     (dict(n=4096, block=4, levels=2), -2),  # B != 16
+                     (dict(n=2 * 4096), -2)):                # not a square
+        with pytest.raises(llsa.LLSAError) as e:
+            llsa.get_sizes(llsa.Params(1, 1, d=64, token_order="raster", **kw))
+        assert e.value.code == code
+    # raster order takes the per-query-block forward: no grouping workspace
+    assert llsa.workspace_bytes(llsa.Params(1, 12, 65536, 64, token_order="raster"), llsa.OP_FWD) == 0
+    p = llsa.Params(1, 1, 4096, 64).c()
+    p.token_order = 2  # no such order
+    assert lib.llsa_get_sizes(ctypes.byref(p), ctypes.byref(llsa._Sizes())) == -1
+    with pytest.raises(ValueError):
+        llsa.Params(1, 1, 4096, 64, token_order="zorder").c()
