@@ -501,7 +501,8 @@ def run_llsa(args, ws, rank, local):
     if rank == 0 and ws == 1:
         out["reorder"] = reorder_rate(w, dev, peaks)
         out["routing_recall"] = routing_recall(p, b, w, dev)
-        out["reorder_in_step"] = reorder_in_step(w, d, ms_step, dev)
+        if not args.no_reorder:
+            out["reorder_in_step"] = reorder_in_step(w, d, ms_step, dev)
     if rank == 0 and ws == 1 and not args.no_dense:
         out["dense_sdpa"] = dense_comparator(w, dev, ms_step)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -819,6 +820,7 @@ def main():
     ap.add_argument("--workload", default=synth.HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
+    ap.add_argument("--no-reorder", action="store_true", help="skip the index-reordering steps after the timed region")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture of this build")
     ap.add_argument("--sweep", action="store_true",
