@@ -47,7 +47,7 @@ int launch_coarse_reduce(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_bwd_dkv_simt(const Shape& s, const AttnArgs& a, cudaStream_t st);
 
 // groups of query blocks sharing their selected key blocks (group.cu) and the
-// grouped tensor-core forward over them (bf16, B = 16, d = 64, K_1 in {8, 16})
+// grouped tensor-core forward over them (bf16, B = 16, d = 64, K_1 in {4, 8, 16})
 bool group_supported(const Shape& s);
 constexpr int kGroupWindow = 1024;  // query blocks per grouping window
 int group_windows(const Shape& s);    // grouping windows per slice
@@ -106,12 +106,13 @@ __device__ __forceinline__ long long sum_groups(const int32_t* ngroups, long lon
 int launch_fwd_grp(const Shape& s, const AttnArgs& a, const int32_t* ngroups, const GroupRec* recs,
                    cudaStream_t st);
 
-// tensor-core kernels (bf16, B = 16, d in {64, 128}, K_1 in {8, 16})
+// per-query-block tensor-core forward (bf16, B = 16, d in {64, 128} with K_1 in
+// {8, 16}, d = 64 with K_1 = 32)
 bool fwd_tc_supported(const Shape& s);
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
 int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);
 // the tensor-core backward (dQ and dK/dV kernels): bf16, B = 16, d in {64, 128},
-// K_1 in {4, 8, 16}, one enrichment column per level
+// K_1 in {4, 8, 16} (and 32 at d = 64), one enrichment column per level
 bool bwd_tc_supported(const Shape& s);
 bool bwd_dkv_tc_fits(const Shape& s);
 int launch_bwd_dkv_tc(const Shape& s, const AttnArgs& a, cudaStream_t st);

@@ -1,5 +1,6 @@
 // attn_bwd_dq_tc.cu -- backward, query-major part, on the tcgen05 tensor cores
-// (bf16, B = 16, d in {64, 128}, K_1 in {4, 8, 16}): dq, D = rowsum(dO o) (stored
+// (bf16, B = 16, d in {64, 128}, K_1 in {4, 8, 16}, and K_1 = 32 at d = 64):
+// dq, D = rowsum(dO o) (stored
 // with lse as (lse, D) pairs for the key-major kernel), and
 // the per-(query block, level) partial gradients of the pooled keys and values.
 //
@@ -69,7 +70,12 @@ struct Cfg {
     static constexpr int STAGES_RAW = (kSmemBudget - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 6 ? 6 : STAGES_RAW;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
-    static constexpr int TM_GROUP = 128;  // per warpgroup: S +0, dP +32, dq +64, gK +96, gV +112
+    // TMEM columns per warpgroup: S +0 and dP (16 per key tile each), then dq,
+    // gK, gV (16 each); up to two key tiles S +0, dP +32, dq +64, gK +96, gV +112
+    static constexpr int TM_DP = NT <= 2 ? 32 : NT * 16;
+    static constexpr int TM_DQ = 2 * TM_DP, TM_GK = TM_DQ + 32, TM_GV = TM_DQ + 48;
+    static constexpr int TM_GROUP = NT <= 2 ? 128 : 256;
+    static constexpr int TM_ALLOC = 2 * TM_GROUP;
 };
 
 struct Misc {
@@ -124,7 +130,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     for (int x = threadIdx.x; x < 4 * C::BC_BYTES / 16; x += kThreads)
         reinterpret_cast<uint4*>(bcbuf)[x] = make_uint4(0u, 0u, 0u, 0u);
     fence_async_smem();
-    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), 256);
+    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), C::TM_ALLOC);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -257,7 +263,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
                     const uint32_t qoff = (ks / 4) * 2048 + (ks % 4) * 32;
                     mma_bf16_warp(tbase + w * C::TM_GROUP + t * 16, dKm + ((s0 + C::OFF_K + koff) >> 4),
                                   dKm + ((s0 + qoff) >> 4), idS, ks > 0);
-                    mma_bf16_warp(tbase + w * C::TM_GROUP + 32 + t * 16, dKm + ((s0 + C::OFF_V + koff) >> 4),
+                    mma_bf16_warp(tbase + w * C::TM_GROUP + C::TM_DP + t * 16, dKm + ((s0 + C::OFF_V + koff) >> 4),
                                   dKm + ((s0 + C::OFF_DO + qoff) >> 4), idS, ks > 0);
                 }
             mma_commit_warp(smem_u32(&ms->s_full[w]));
@@ -272,10 +278,10 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             const uint32_t tg = tbase + w * C::TM_GROUP;
 #pragma unroll
             for (int ks = 0; ks < C::NF / 16; ks++)
-                mma_bf16_warp(tg + 64, dMN + ((s0 + C::OFF_K + ks * 2048) >> 4),
+                mma_bf16_warp(tg + C::TM_DQ, dMN + ((s0 + C::OFF_K + ks * 2048) >> 4),
                               dDS + ((d0 + (ks / 4) * 2048 + (ks % 4) * 32) >> 4), idQ, ks > 0);
-            mma_bf16_warp(tg + 96, dQT + (s0 >> 4), dBC + (b0 >> 4), idQ, 0);
-            mma_bf16_warp(tg + 112, dQT + ((s0 + C::OFF_DO) >> 4), dBC + ((b0 + C::BC_BYTES) >> 4), idQ, 0);
+            mma_bf16_warp(tg + C::TM_GK, dQT + (s0 >> 4), dBC + (b0 >> 4), idQ, 0);
+            mma_bf16_warp(tg + C::TM_GV, dQT + ((s0 + C::OFF_DO) >> 4), dBC + ((b0 + C::BC_BYTES) >> 4), idQ, 0);
             mma_commit_warp(smem_u32(&ms->g_full[w]));
             mma_commit_warp(smem_u32(&ms->empty[st]));
         };
@@ -430,7 +436,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             for (int t = 0; t < NT; t++) {
                 float s[16], dp[16];
                 tmem_ld16(tS + t * 16, s);
-                tmem_ld16(tS + 32 + t * 16, dp);
+                tmem_ld16(tS + C::TM_DP + t * 16, dp);
                 // an M = 128 tile holds key qr * 32 + lane in this thread's TMEM
                 // lane; an M = 64 tile (K_1 = 4) holds key 16 qr + lane in lanes
                 // 0-15 of each quarter
@@ -454,9 +460,9 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
             mbar_wait(smem_u32(&ms->g_full[w]), j & 1, abort_flag, a.status, a.spin);
             tc_fence_after();
             float q[16], gk[16], gv[16];
-            tmem_ld16(tS + 64, q);
-            tmem_ld16(tS + 96, gk);
-            tmem_ld16(tS + 112, gv);
+            tmem_ld16(tS + C::TM_DQ, q);
+            tmem_ld16(tS + C::TM_GK, gk);
+            tmem_ld16(tS + C::TM_GV, gv);
             tc_fence_before();
             mbar_arrive(smem_u32(&ms->o_free[w]));
             if (valid) {
@@ -491,7 +497,7 @@ bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tbase, 256);
+        tmem_dealloc(tbase, C::TM_ALLOC);
     }
 }
 
@@ -523,6 +529,7 @@ int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     for (int t = 0; t < 5; t++) LLSA_TRY(make_tmap_tokens(&maps[t], bases[t], s));
     if (s.d == 64) {
         if (s.K1 == 4) return launch_cfg<64, 64>(s, a, maps, st);
+        if (s.K1 == 32) return launch_cfg<64, 512>(s, a, maps, st);
         return s.K1 == 8 ? launch_cfg<64, 128>(s, a, maps, st) : launch_cfg<64, 256>(s, a, maps, st);
     }
     if (s.K1 == 4) return launch_cfg<128, 64>(s, a, maps, st);
@@ -531,7 +538,7 @@ int launch_bwd_dq_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
 
 bool bwd_tc_supported(const Shape& s) {
     return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && (s.d == 64 || s.d == 128) &&
-           (s.K1 == 4 || s.K1 == 8 || s.K1 == 16) && s.Le <= 4 && s.Lc == s.Le &&
+           (s.K1 == 4 || s.K1 == 8 || s.K1 == 16 || (s.K1 == 32 && s.d == 64)) && s.Le <= 4 && s.Lc == s.Le &&
            s.slices * (long long)s.n < (1LL << 31) && bwd_dkv_tc_fits(s);
 }
 

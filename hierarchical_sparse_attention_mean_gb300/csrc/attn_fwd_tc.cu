@@ -1,6 +1,7 @@
 // attn_fwd_tc.cu -- block-sparse attention forward with KV enrichment on the
 // tcgen05 tensor cores (bf16 in, fp32 accumulate), for B = 16, d in {64, 128}
-// and K_1 in {8, 16} (128 or 256 fine keys per query block).
+// and K_1 in {8, 16} (128 or 256 fine keys per query block), and K_1 = 32 at
+// d = 64 (512 keys: four key tiles, one ring stage).
 //
 // Method: Pith review of arXiv 2512.16615, "Core claim": every query block of
 // B tokens attends the B tokens of its K selected blocks plus one pooled K/V
@@ -65,7 +66,10 @@ struct Cfg {
     static constexpr int SPP = (STAGES_RAW < 1 ? 1 : (STAGES_RAW > 6 ? 6 : STAGES_RAW)) / NPROD;
     static constexpr int STAGES = NPROD * SPP;
     static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + FIXED;
-    static constexpr int TM_GROUP = 64;          // TMEM columns per warpgroup: S at +0, O at +32
+    // TMEM columns per warpgroup: S at +0 (16 per key tile), O after it
+    static constexpr int TM_O = NT <= 2 ? 32 : NT * 16;
+    static constexpr int TM_GROUP = NT <= 2 ? 64 : 128;
+    static constexpr int TM_ALLOC = 2 * TM_GROUP;
 };
 
 // Block bl of a CTA goes to gather warp bl % NPROD; within that warp's
@@ -138,7 +142,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         (&ms->cs[0][0][0])[x] = -INFINITY;
         (&ms->ecs[0][0][0])[x] = 0.f;
     }
-    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), 128);
+    if (warp == 1) tmem_alloc(smem_u32(&ms->tmem_slot), C::TM_ALLOC);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -269,7 +273,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 const uint32_t p0 = (uint32_t)(w * C::P_BYTES);
 #pragma unroll
                 for (int ks = 0; ks < C::NF / 16; ks++)
-                    mma_bf16(tbase + w * C::TM_GROUP + 32, dV + ((v0 + ks * 2048) >> 4),
+                    mma_bf16(tbase + w * C::TM_GROUP + C::TM_O, dV + ((v0 + ks * 2048) >> 4),
                              dP + ((p0 + (ks / 4) * 2048 + (ks % 4) * 32) >> 4), idPV, ks > 0);
                 mma_commit(smem_u32(&ms->o_full[w]));
                 mma_commit(smem_u32(&ms->empty[st]));
@@ -303,7 +307,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const int w = (warp - 4) >> 2, qr = warp & 3;
         const int tw = threadIdx.x - 128 * (1 + w);
         const uint32_t tS = tbase + w * C::TM_GROUP + ((uint32_t)(qr * 32) << 16);
-        const uint32_t tO = tS + 32;
+        const uint32_t tO = tS + C::TM_O;
         const float sc = a.scale, scl2 = a.scale * kLog2e;
         const int dd = D == 64 ? 16 * qr + lane : 32 * qr + lane;  // O^T row this thread reads back
         const bool valid = D == 64 ? lane < 16 : true;
@@ -463,7 +467,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tbase, 128);
+        tmem_dealloc(tbase, C::TM_ALLOC);
     }
 }
 
@@ -1020,8 +1024,10 @@ int launch_any(const Shape& s, const AttnArgs& a, const CUtensorMap& mq, const C
 
 bool fwd_tc_supported(const Shape& s) {
     // one enrichment column per level (the pooled keys sit in four row slots)
-    return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && (s.d == 64 || s.d == 128) && (s.K1 == 8 || s.K1 == 16) &&
-           s.Le <= 4 && s.Lc == s.Le && s.slices * (long long)s.n < (1LL << 31);
+    // (K_1 = 32 at d = 64: four key tiles, one ring stage)
+    return s.dtype == LLSA_DTYPE_BF16 && s.B == 16 && (s.d == 64 || s.d == 128) &&
+           (s.K1 == 8 || s.K1 == 16 || (s.K1 == 32 && s.d == 64)) && s.Le <= 4 && s.Lc == s.Le &&
+           s.slices * (long long)s.n < (1LL << 31);
 }
 
 int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
@@ -1029,7 +1035,10 @@ int launch_fwd_tc(const Shape& s, const AttnArgs& a, cudaStream_t st) {
     LLSA_TRY(make_tmap_tokens(&mq, a.q, s));
     LLSA_TRY(make_tmap_tokens(&mk, a.k, s));
     LLSA_TRY(make_tmap_tokens(&mv, a.v, s));
-    if (s.d == 64) return s.K1 == 8 ? launch_any<64, 1>(s, a, mq, mk, mv, st) : launch_any<64, 2>(s, a, mq, mk, mv, st);
+    if (s.d == 64) {
+        if (s.K1 == 32) return launch_any<64, 4>(s, a, mq, mk, mv, st);
+        return s.K1 == 8 ? launch_any<64, 1>(s, a, mq, mk, mv, st) : launch_any<64, 2>(s, a, mq, mk, mv, st);
+    }
     return s.K1 == 8 ? launch_any<128, 1>(s, a, mq, mk, mv, st) : launch_any<128, 2>(s, a, mq, mk, mv, st);
 }
 

@@ -75,8 +75,9 @@ enum { LLSA_ENRICH_TOP1 = 0, LLSA_ENRICH_ANCESTOR = 1, LLSA_ENRICH_ALLK = 2 };
  * sqrt(N); pool, forward and backward read and write them in place of a
  * reordering pass, working in tile order inside. Needs B = 16 and a side of
  * 4^m (LLSA_ERR_SHAPE otherwise); llsa_fwd and llsa_bwd take it only on the
- * per-query-block tensor-core kernels (bf16, d in {64, 128}, K_1 in {8, 16},
- * one coarse token per level; the forward needs no workspace then), else
+ * per-query-block tensor-core kernels (bf16, d in {64, 128} with K_1 in
+ * {8, 16}, or d = 64 with K_1 = 32; one coarse token per level; the forward
+ * needs no workspace then), else
  * LLSA_ERR_UNSUPPORTED. Everything that is not a token
  * tensor keeps the tile order: pyr, lse, sel_idx, coarse_idx, level_idx,
  * col_ptr and row_idx index blocks and tokens by tile position. */
@@ -168,11 +169,13 @@ int llsa_select(const llsa_params *p, const float *pyr, int32_t *sel_idx, int32_
  *                query blocks that share selected key blocks, which the
  *                grouped tensor-core forward gathers once per group. Too
  *                small a workspace: LLSA_ERR_WORKSPACE, nothing enqueued.
- * Where the grouped forward applies (bf16, B = 16, d = 64, K_1 in {8, 16},
+ * Where the grouped forward applies (bf16, B = 16, d = 64, K_1 in {4, 8, 16},
  * one enrichment column per level, L_e <= 3), the call groups the query blocks
  * first and then takes the grouped forward when the groups hold at least 4.5
  * query blocks on average, else the per-query-block one (decided on the
- * device; both agree within rounding).
+ * device; both agree within rounding; K_1 = 4 has only the grouped one). The
+ * per-query-block tensor-core forward takes d in {64, 128} with K_1 in {8, 16},
+ * and d = 64 with K_1 = 32; other shapes run on CUDA-core kernels.
  * A key block listed twice in a row of sel_idx counts once (the key set is
  * the union of the listed blocks). */
 int llsa_fwd(const llsa_params *p, const void *q, const void *k, const void *v, const float *pyr,

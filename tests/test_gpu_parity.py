@@ -32,6 +32,9 @@ CASES = {
     # d = 128 takes the CUDA-core forward and the tensor-core backward
     "d64-K4": W("d64k4", 1, 3, 4096, 64, topk=4, amplitude=0.5, seed=84),
     "d128-K4-grf": W("d128k4", 1, 2, 4096, 128, topk=4, kind="grf", length_scale=4.0, grid=(64, 64), seed=85),
+    # K_1 = 32 (512 fine keys per query block): four key tiles with one ring
+    # stage in the per-block forward and in dQ
+    "d64-K32-grf": W("d64k32", 1, 2, 4096, 64, topk=32, kind="grf", length_scale=4.0, grid=(64, 64), seed=86),
     "B4-L4-fp32": W("b4", 1, 2, 1024, 32, block=4, topk=3, dtype="fp32", seed=79),
     "B2-fig1": W("fig1", 1, 1, 8, 8, block=2, topk=1, dtype="fp32", seed=80),
     "B8-d16-bf16": W("b8", 2, 1, 512, 16, block=8, topk=5, amplitude=0.5, seed=81),

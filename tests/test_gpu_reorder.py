@@ -85,6 +85,7 @@ def _step(p, x, flags=0):
     (1, 2, 64, 64, 16),
     (1, 2, 64, 128, 8),
     (1, 2, 64, 128, 16),
+    (1, 2, 64, 64, 32),                                 # four key tiles per query block
     (1, 2, 256, 64, 8),                                 # 256 x 256 pixel tokens, three levels
 ])
 def test_raster_order_step_equals_step_on_reordered_tokens(b, h, side, d, K):
