@@ -336,6 +336,10 @@ def run_llsa(args, ws, rank, local):
         llsa.forward(p, d["q"], d["k"], d["v"], b)
         llsa.backward(p, d["q"], d["k"], d["v"], d["dout"], b, dq, dk, dv)
 
+    forced = {"auto": 0, "grouped": llsa.LLSA_TEST_FORCE_GROUPED,
+              "per_block": llsa.LLSA_TEST_FORCE_PER_BLOCK}[args.forward]
+    if forced:
+        llsa.test_set_wait_limit(0, forced)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -485,6 +489,7 @@ def run_llsa(args, ws, rank, local):
                    "keys_per_query": s.keys_per_query, "inputs": f"{w.kind}, seed {w0.seed} (+7919 per rank)",
                    "l2": "no flush: the step's inputs (4 x %.0f MB) exceed the 129 MB L2" % (h2d / 4 / 1e6),
                    "parallelism": f"replicas{ws}", "step": "pool+select+fwd+transpose+bwd",
+                   "forward": args.forward,
                    "flops_per_step": work["step_flops"], "flops_counted": "14*d per (query, key) pair: "
                    "fwd 4d, bwd 10d (S, dP, dV, dK, dQ); selection excluded"},
         "stage_ms": stage_ms,
@@ -821,6 +826,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparator")
     ap.add_argument("--no-reorder", action="store_true", help="skip the index-reordering steps after the timed region")
+    ap.add_argument("--forward", choices=["auto", "grouped", "per_block"], default="auto",
+                    help="which tensor-core forward runs: the library's choice per call (default), or one of the "
+                         "two forced (for comparing them; both compute the same outputs)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture of this build")
     ap.add_argument("--sweep", action="store_true",
