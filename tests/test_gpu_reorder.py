@@ -161,3 +161,49 @@ def test_raster_order_outside_the_tensor_core_path_is_refused():
         assert e.value.code == -8
     torch.cuda.synchronize()
     assert llsa.llsa_get_status() == 0
+
+
+def test_raster_order_pool_fp32_equals_pool_on_reordered_tokens():
+    """The fp32 pool reads raster tokens as 4 x 4 patches in the same order
+    as the tile-order pool reads the permuted tokens: the pyramids are equal."""
+    side, d = 64, 32
+    n = side * side
+    g = torch.Generator().manual_seed(5)
+    x = {k: torch.randn(1, 2, n, d, generator=g) for k in ("q", "k", "v")}
+    src = torch.from_numpy(oracle.tile_order(side, side, 16))
+    pr = llsa.Params(1, 2, n, d, dtype="fp32", token_order="raster")
+    pt = llsa.Params(1, 2, n, d, dtype="fp32")
+    s = llsa.get_sizes(pt)
+    out = []
+    for p, xs in ((pr, x), (pt, {k: t[:, :, src].contiguous() for k, t in x.items()})):
+        dev = {k: t.cuda() for k, t in xs.items()}
+        pyr = torch.empty(3, 2, s.pyr_rows, d, device="cuda")
+        llsa.llsa_pool(p, dev["q"], dev["k"], dev["v"], pyr)
+        out.append(pyr)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], out[1])
+
+
+def test_raster_order_autograd():
+    """llsa_attention with token_order="raster": output and input gradients
+    equal the tile-order call on permuted tokens (per-block forward forced on
+    both, so the arithmetic is the same)."""
+    x = _raster_inputs(1, 2, 64, 64, seed=91)
+    src = torch.from_numpy(oracle.tile_order(64, 64, 16)).cuda()
+    res = []
+    llsa.test_set_wait_limit(0, llsa.LLSA_TEST_FORCE_PER_BLOCK)
+    try:
+        for order in ("raster", "tile"):
+            t = {k: v.cuda() for k, v in x.items()}
+            if order == "tile":
+                t = {k: v[:, :, src].contiguous() for k, v in t.items()}
+            q, k, v = (t[n].requires_grad_(True) for n in ("q", "k", "v"))
+            o = llsa.llsa_attention(q, k, v, token_order=order)
+            o.backward(t["dout"])
+            res.append((o.detach(), q.grad, k.grad, v.grad))
+        torch.cuda.synchronize()
+    finally:
+        llsa.test_set_wait_limit(0, 0)
+    assert llsa.llsa_get_status() == 0
+    for got, ref in zip(res[0], res[1]):
+        assert torch.equal(got[:, :, src], ref)
