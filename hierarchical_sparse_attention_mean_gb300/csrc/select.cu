@@ -22,6 +22,10 @@
 // unsigned keys, so a round is one warp max-reduction of the key and one
 // min-reduction of the index among the lanes holding that key. K <= 64 and
 // C <= 1024 here, so K rounds cost less than a full sort of the C candidates.
+// With 16 or more candidates per lane (K_{l+1} B >= 512) the K-th largest key
+// is found instead by a 32-step binary search on the key bits (one warp sum
+// per step), and the row keeps every key above it plus the lowest indices
+// among the ties.
 #include <limits.h>
 
 #include "internal.h"
@@ -184,20 +188,55 @@ __global__ void __launch_bounds__(32 * kMaxRows, CPL <= 8 ? (DT > 0 ? 3 : 4) : 1
             if (lane == 0) krow[k] = wi;
         }
     } else {
-        unsigned taken = 0;
-        for (int k = 0; k < a.Kl; k++) {
-            unsigned bk = 0u;
-            int bi = INT_MAX;
+        // 16 or more candidates per lane: a threshold select instead of K
+        // rounds. T = the K-th largest key counted with multiplicity, found
+        // bit by bit from the top (the largest T with at least K keys >= T;
+        // padding keys are 0, below every score). The kept set is every key
+        // above T, then the lowest indices among the keys equal to T: the same
+        // set the rounds keep.
+        unsigned T = 0u;
+        for (int bit = 31; bit >= 0; bit--) {
+            const unsigned t = T | (1u << bit);
+            unsigned cnt = 0;
 #pragma unroll
-            for (int m = 0; m < CPL; m++)
-                if (!(taken >> m & 1u) && (key[m] > bk || (key[m] == bk && idx[m] < bi))) { bk = key[m]; bi = idx[m]; }
-            const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
-            const int wi = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bi : 0xffffffffu);
-#pragma unroll
-            for (int m = 0; m < CPL; m++)
-                if (idx[m] == wi) taken |= 1u << m;
-            if (lane == 0) krow[k] = wi;
+            for (int m = 0; m < CPL; m++) cnt += key[m] >= t ? 1u : 0u;
+            if ((int)__reduce_add_sync(0xffffffffu, cnt) >= a.Kl) T = t;
         }
+        bool sel[CPL];
+        unsigned above = 0;
+#pragma unroll
+        for (int m = 0; m < CPL; m++) {
+            sel[m] = key[m] > T;
+            above += sel[m] ? 1u : 0u;
+        }
+        for (int need = a.Kl - (int)__reduce_add_sync(0xffffffffu, above); need > 0; need--) {
+            unsigned bi = 0xffffffffu;
+#pragma unroll
+            for (int m = 0; m < CPL; m++)
+                if (!sel[m] && key[m] == T && (unsigned)idx[m] < bi) bi = (unsigned)idx[m];
+            const unsigned wi = __reduce_min_sync(0xffffffffu, bi);
+#pragma unroll
+            for (int m = 0; m < CPL; m++)
+                if (!sel[m] && key[m] == T && (unsigned)idx[m] == wi) sel[m] = true;
+        }
+        // rank 1 (the largest key, the lowest index among equal ones; always
+        // kept) first, then the others in lane order
+        unsigned bk = 0u;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int m = 0; m < CPL; m++)
+            if (key[m] > bk || (key[m] == bk && idx[m] < bi)) { bk = key[m]; bi = idx[m]; }
+        const unsigned wk = __reduce_max_sync(0xffffffffu, bk);
+        const int w1 = (int)__reduce_min_sync(0xffffffffu, bk == wk ? (unsigned)bi : 0xffffffffu);
+        int base = 1;
+#pragma unroll
+        for (int m = 0; m < CPL; m++) {
+            const bool put = sel[m] && idx[m] != w1;
+            const unsigned bits = __ballot_sync(0xffffffffu, put);
+            if (put) krow[base + __popc(bits & ((1u << lane) - 1u))] = idx[m];
+            base += __popc(bits);
+        }
+        if (lane == 0) krow[0] = w1;
     }
     __syncwarp();
     const int row = row0 + warp;

@@ -35,6 +35,9 @@ CASES = {
     # K_1 = 32 (512 fine keys per query block): four key tiles with one ring
     # stage in the per-block forward and in dQ
     "d64-K32-grf": W("d64k32", 1, 2, 4096, 64, topk=32, kind="grf", length_scale=4.0, grid=(64, 64), seed=86),
+    # 512 level-1 candidates per row (16 per lane): the selection's threshold
+    # form of the Top-K
+    "n16384-K32": W("n16k32", 1, 2, 16384, 64, topk=32, amplitude=0.5, seed=87),
     "B4-L4-fp32": W("b4", 1, 2, 1024, 32, block=4, topk=3, dtype="fp32", seed=79),
     "B2-fig1": W("fig1", 1, 1, 8, 8, block=2, topk=1, dtype="fp32", seed=80),
     "B8-d16-bf16": W("b8", 2, 1, 512, 16, block=8, topk=5, amplitude=0.5, seed=81),
@@ -176,10 +179,16 @@ def test_end_to_end(case_data, name):
 
 # ------------------------------------------------------------ edge cases
 
-def test_constant_inputs_tie_break_bit_exact():
-    """Every score ties: the lower index wins at every level, on both sides."""
-    w = W("const", 1, 2, 4096, 64, seed=1)
-    x = {k: np.full((2, 4096, 64), 0.5, np.float32) for k in ("q", "k", "v", "dout")}
+@pytest.mark.parametrize("n,K,g", [(4096, 8, 0.5), (16384, 32, 0.02)])
+def test_constant_inputs_tie_break_bit_exact(n, K, g):
+    """Every score ties: the lower index wins at every level, on both sides
+    (at 16,384 tokens with K = 32 through the threshold form of the Top-K).
+    Every query block then selects the same key blocks, so dv of those keys
+    sums all N queries; the output gradient g keeps it near 1 there (with 0.5
+    it reaches about 31, where one bf16 step is 0.125, above the bf16 bound)."""
+    w = W("const", 1, 2, n, 64, topk=K, seed=1)
+    x = {k: np.full((2, n, 64), 0.5, np.float32) for k in ("q", "k", "v")}
+    x["dout"] = np.full((2, n, 64), g, np.float32)
     ref = run_oracle(w, x)
     out, _ = gpu_stage_outputs(w, x)
     for s, r in enumerate(ref["slices"]):
